@@ -1,0 +1,182 @@
+/*
+ * moe_w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 routed-expert MoE layer.
+ *
+ * One handle = one MoE FFN layer: a router [E, H] applied to FP16 activations,
+ * top-k expert selection, and E experts whose gate/up [I, H] and down [H, I]
+ * weights stay compact (signed int4, one FP16 scale per 256 consecutive K
+ * values) in a fixed pool of GPU "slots".  No expanded FP16 copy of an expert
+ * is ever kept: kernels dequantise the values they need while computing.
+ *
+ * Sources (Horizon RunMap pages):
+ *  - "Horizon RunMap - architecture", section "Representation and
+ *    computation": routed experts INT4 qpacked with 256-value blocks and FP16
+ *    scales; compact weights on the GPU; FP16 activations; no persistent
+ *    expanded expert (temporary kernel values and workspaces are separate).
+ *  - same page, section "Immutable authority and miss lifecycle": capacity is
+ *    fixed before admission (here: everything is sized at create).
+ *  - same page, section "Regimes and executor boundaries": a resident expert
+ *    need not be routed (slots and the expert->slot table are separate).
+ *  - landing page (/en), section "08 / Precision & quality": values converted
+ *    in-kernel, FP32 accumulation stages and explicit rounding; routing
+ *    stays outside INT4.
+ *
+ * Canonical "qpacked" layout accepted by moe_w4a16_pack_experts, per expert,
+ * experts concatenated along the leading axis:
+ *   gate_q, up_q : uint8  [I][H/2]          gate_s, up_s : fp16 bits [I][ceil(H/256)]
+ *   down_q       : uint8  [H][I/2]          down_s       : fp16 bits [H][ceil(I/256)]
+ * Rows are output features, K (the reduction index) is contiguous; byte b of a
+ * row holds K index 2b in its low nibble and 2b+1 in its high nibble; each
+ * nibble is a two's-complement int4 in [-8, 7]; w[r][k] = q[r][k] * s[r][k/256]
+ * (no zero-point; the last block of a row may be shorter than 256).
+ *
+ * Layer computed by moe_w4a16_forward for x [T][H] (FP16):
+ *   xin   = PRENORM ? x / sqrt(mean_h x^2 + 1e-6) : x          (per token)
+ *   l     = xin . W_r^T + bias                                 (FP32)
+ *   p     = softmax(l) over all E;  ids = the k largest l (ties -> lower
+ *           expert index), largest first;  w_j = p[ids_j] (not renormalised)
+ *   y_j   = W_d (SiLU(W_g xin) * (W_u xin))   for expert ids_j
+ *   out   = (RESIDUAL ? x : 0) + sum_{j=0..k-1} w_j y_j        (FP32, j order)
+ * rounded to FP16 at two points: the SiLU*up product h (the A16 operand of the
+ * down projection) and the final out.  Dequantised weights are formed as the
+ * FP16 value nearest q*s.  A routed expert whose slot is absent contributes 0
+ * and is counted as a miss (see moe_w4a16_get_status).
+ *
+ * Threading: a handle is not thread-safe; calls on one handle must be
+ * serialised by the caller.  Asynchrony: every call taking a cudaStream_t
+ * only enqueues work on that stream (after synchronous argument checks);
+ * device buffers passed in must stay valid until the stream reaches the call.
+ * forward enqueues no allocation, no host synchronisation and no
+ * host<->device copy, so it may be captured in a CUDA graph.
+ *
+ * Errors: argument, shape and state errors are returned synchronously and
+ * nothing is enqueued.  Conditions only the device can see (a routed expert
+ * that has no slot; a bounded wait that gave up) are recorded in a device
+ * status word read by moe_w4a16_get_status.  The library never aborts or
+ * traps.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_W4A16_API __attribute__((visibility("default")))
+#else
+#define MOE_W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_w4a16_stream_t;   /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOE_W4A16_OK = 0,
+  MOE_W4A16_ERR_INVALID_ARG = 1,   /* bad pointer, shape, index or flag */
+  MOE_W4A16_ERR_CUDA = 2,          /* a CUDA runtime call failed (message in last_error) */
+  MOE_W4A16_ERR_OOM = 3,           /* device allocation failed at create */
+  MOE_W4A16_ERR_NOT_PACKED = 4,    /* the slot table names a slot never packed */
+  MOE_W4A16_ERR_NOT_RESIDENT = 5,  /* get_status: a routed expert had no slot */
+  MOE_W4A16_ERR_TIMEOUT = 6,       /* get_status: a bounded device wait gave up */
+  MOE_W4A16_ERR_UNSUPPORTED = 7    /* valid request this build does not implement */
+} moe_w4a16_status;
+
+/* forward flags */
+#define MOE_W4A16_RESIDUAL   1u   /* out = x + MoE(...) */
+#define MOE_W4A16_PRENORM    2u   /* experts and router see x / rms(x) */
+#define MOE_W4A16_FORCE_GEMV 4u   /* decode kernels whatever T is */
+#define MOE_W4A16_FORCE_GEMM 8u   /* tensor-core grouped GEMM whatever T is */
+
+typedef struct {
+  int32_t hidden;       /* H: multiple of 64, >= 64 */
+  int32_t inter;        /* I: expert intermediate size, multiple of 64, >= 64 */
+  int32_t num_experts;  /* E: 1..256 */
+  int32_t top_k;        /* k: 1..min(E, 32) */
+  int32_t num_slots;    /* S: GPU pool rows, 1..65535 */
+  int32_t max_tokens;   /* upper bound on T for every forward, >= 1 */
+  int32_t device;       /* CUDA device ordinal */
+} moe_w4a16_config;
+
+typedef struct moe_w4a16_handle moe_w4a16_handle;
+
+/* Allocates the slot pool (S rows of the kernel-internal compact layout),
+ * the expert->slot table and every forward workspace, sized from cfg.  No
+ * slot is packed and the table maps every expert to "absent" until set.
+ * On success *out receives the handle; on failure *out is NULL.  H or I that
+ * is odd gives ERR_INVALID_ARG; even but not a multiple of 64 gives
+ * ERR_UNSUPPORTED. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle** out);
+
+/* Waits for the handle's device work, frees everything it owns.  NULL is OK. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_destroy(moe_w4a16_handle* h);
+
+/* Writes n experts, given in the canonical layout above, into slots
+ * [slot0, slot0 + n).  The six arrays may be host or device pointers (the
+ * kind is detected per array); host memory is copied synchronously through a
+ * handle-owned device staging buffer, device memory is read on `stream`.
+ * The pool keeps the compact 4-bit form (re-ordered for the kernels; still
+ * 4 bits per weight plus the FP16 scales).  The caller's arrays may be freed
+ * once the stream has passed this call. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_pack_experts(moe_w4a16_handle* h, int32_t slot0, int32_t n,
+                                        const uint8_t* gate_q, const uint16_t* gate_s,
+                                        const uint8_t* up_q, const uint16_t* up_s,
+                                        const uint8_t* down_q, const uint16_t* down_s,
+                                        moe_w4a16_stream_t stream);
+
+/* expert_to_slot: HOST array [E]; entry e is the slot holding expert e, or -1
+ * if expert e is not resident.  Rejected (nothing changes): an entry outside
+ * [-1, S), two experts on one slot (ERR_INVALID_ARG), or a slot that was
+ * never packed (ERR_NOT_PACKED).  The table is uploaded on `stream`, so
+ * forwards enqueued after this call on that stream see it. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_set_slot_table(moe_w4a16_handle* h, const int32_t* expert_to_slot,
+                                          moe_w4a16_stream_t stream);
+
+/* One layer forward on `stream`.
+ *   x        : device FP16 [T][H]        router_w : device FP16 [E][H]
+ *   bias     : device FP32 [E] or NULL   (may hold -inf)
+ *   out      : device FP16 [T][H]        (must not alias x)
+ * Optional device outputs (NULL to skip), written in the same call:
+ *   topk_ids [T][k] int32, topk_w [T][k] FP32,
+ *   sorted_pairs [T*k] int32 (flat pair index p = t*k + j, grouped by expert
+ *   ascending and by p ascending inside a group), expert_offsets [E+1] int32.
+ * x, router_w and out must be 16-byte aligned (ERR_INVALID_ARG otherwise).
+ * 0 <= T <= max_tokens; T == 0 enqueues nothing and returns OK.  FORCE_GEMV
+ * and FORCE_GEMM are mutually exclusive. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T,
+                                   const void* router_w, const float* bias, uint32_t flags,
+                                   void* out, int32_t* topk_ids, float* topk_w,
+                                   int32_t* sorted_pairs, int32_t* expert_offsets,
+                                   moe_w4a16_stream_t stream);
+
+/* Same layer with HOST activations: copies x_host (FP16 [T][H]) into a
+ * handle-owned device buffer, runs moe_w4a16_forward, copies the result into
+ * out_host (FP16 [T][H]) and synchronises `stream` before returning.  Host
+ * buffers should be page-locked for the copies to be asynchronous. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_host(moe_w4a16_handle* h, const void* x_host, int32_t T,
+                                        const void* router_w, const float* bias, uint32_t flags,
+                                        void* out_host, moe_w4a16_stream_t stream);
+
+/* Synchronises the handle's device, reads and clears the device status word.
+ * *miss_count (may be NULL) receives the number of routed token-expert pairs
+ * whose expert had no slot since the last call.  Returns ERR_TIMEOUT if a
+ * bounded wait gave up, else ERR_NOT_RESIDENT if there was a miss, else OK. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t* miss_count);
+
+/* Message of the last error on this handle ("" if none).  With h == NULL,
+ * the message of the last failed create. */
+MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
+
+/* Bytes of one slot row in the pool (compact weights + scales + padding). */
+MOE_W4A16_API size_t moe_w4a16_slot_bytes(const moe_w4a16_handle* h);
+
+/* The largest T the decode (GEMV) kernels take when no FORCE flag is given;
+ * larger T runs the tensor-core grouped GEMM.  Settable for sweeps. */
+MOE_W4A16_API int32_t moe_w4a16_get_gemv_max_tokens(const moe_w4a16_handle* h);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h, int32_t t_star);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4A16_H */

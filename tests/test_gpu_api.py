@@ -1,0 +1,163 @@
+"""Library behaviour on the GPU: edge cases, invariants, misses, errors."""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle
+from tests import gpu_parity as gp
+from w4a16_compact_expert_gb300 import moe_w4a16, synth
+
+pytestmark = pytest.mark.gpu
+F = moe_w4a16
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return synth.tiny_layer()
+
+
+def test_t0_is_noop(tiny):
+    import torch
+    m = gp.make_handle(tiny, 8)
+    try:
+        x = torch.empty(0, 256, dtype=torch.float16, device="cuda")
+        out = m.forward(x, gp.to_dev(tiny.router_w))
+        assert out.shape == (0, 256)
+    finally:
+        m.close()
+
+
+def test_deterministic_and_slot_relabel_invariant(tiny):
+    x = synth.draw_x(7, 33, 256)
+    m = gp.make_handle(tiny, 64)
+    out1, d1 = gp.gpu_forward(m, tiny, x)
+    out2, d2 = gp.gpu_forward(m, tiny, x)
+    m.close()
+    assert np.array_equal(out1, out2) and np.array_equal(d1["sorted_pairs"], d2["sorted_pairs"])
+    # same experts at a permuted set of slot rows (and two spare rows never used)
+    perm = np.array([5, 9, 0, 3, 7, 1, 8, 2])
+    s = tiny.shape
+    m2 = moe_w4a16.MoELayer(s.hidden, s.inter, s.num_experts, s.top_k, num_slots=10, max_tokens=64)
+    try:
+        ex = tiny.experts.arrays()
+        for e in range(8):
+            m2.pack_experts(int(perm[e]), *(a[e:e + 1] for a in ex))
+        m2.pack_experts(4, *(a[:1] for a in ex))
+        m2.pack_experts(6, *(a[1:2] for a in ex))
+        m2.set_slot_table(perm)
+        out3, _ = gp.gpu_forward(m2, tiny, x)
+    finally:
+        m2.close()
+    assert np.array_equal(out1, out3)
+
+
+def test_zero_input_gives_zero(tiny):
+    x = np.zeros((5, 256), np.float16)
+    m = gp.make_handle(tiny, 8)
+    try:
+        out, _ = gp.gpu_forward(m, tiny, x)
+    finally:
+        m.close()
+    assert np.all(out == 0)
+
+
+def test_routed_absent_expert_counts_misses(tiny):
+    x = synth.draw_x(11, 24, 256)
+    table = tiny.expert_to_slot.copy()
+    table[3] = -1
+    table[6] = -1
+    m = gp.make_handle(tiny, 32)
+    try:
+        m.set_slot_table(table)
+        out, dbg = gp.gpu_forward(m, tiny, x)
+        st, miss = m.get_status()
+        st2, miss2 = m.get_status()
+    finally:
+        m.close()
+    ref = moe_oracle.moe_layer(x, tiny.router_w, tiny.bias, tiny.slot_experts().arrays(), 2,
+                               expert_to_slot=table)
+    expected_miss = int(np.isin(ref.ids, [3, 6]).sum())
+    assert expected_miss > 0
+    assert st == F.ERR_NOT_RESIDENT and miss == expected_miss
+    assert st2 == F.OK and miss2 == 0   # cleared by the read
+    keep = ~ref.near_tie
+    gp.assert_output(out, ref.out, keep)
+
+
+def test_dense_single_expert_and_k_equals_e():
+    shape = synth.LayerShape(hidden=128, inter=64, num_experts=1, top_k=1)
+    layer = synth.make_layer(shape, 5)
+    x = synth.draw_x(5, 9, 128)
+    gp.check_full(layer, x, max_tokens=16)
+    shape = synth.LayerShape(hidden=192, inter=128, num_experts=4, top_k=4)
+    layer = synth.make_layer(shape, 6, bias_sigma=0.5)
+    x = synth.draw_x(6, 9, 192)
+    gp.check_full(layer, x, max_tokens=16)
+
+
+def test_forward_host_matches_forward(tiny):
+    x = synth.draw_x(3, 12, 256)
+    m = gp.make_handle(tiny, 16)
+    try:
+        out, _ = gp.gpu_forward(m, tiny, x, F.RESIDUAL)
+        oh = m.forward_host(x, gp.to_dev(tiny.router_w), None, F.RESIDUAL)
+    finally:
+        m.close()
+    assert np.array_equal(out, oh.astype(np.float64))
+
+
+def test_argument_errors(tiny):
+    import torch
+    m = gp.make_handle(tiny, 8)
+    try:
+        x = gp.to_dev(synth.draw_x(1, 9, 256))
+        rw = gp.to_dev(tiny.router_w)
+        with pytest.raises(F.MoEError) as e:
+            m.forward(x, rw)                    # T = 9 > max_tokens = 8
+        assert e.value.status == F.ERR_INVALID_ARG
+        with pytest.raises(F.MoEError) as e:
+            m.forward(x[:2], rw, flags=F.FORCE_GEMM | F.FORCE_GEMV)
+        assert e.value.status == F.ERR_INVALID_ARG
+        with pytest.raises(F.MoEError) as e:
+            m.forward(x[:2], rw, flags=64)
+        assert e.value.status == F.ERR_INVALID_ARG
+        with pytest.raises(F.MoEError) as e:
+            m.set_slot_table([0, 1, 2, 3, 4, 5, 6, 6])
+        assert e.value.status == F.ERR_INVALID_ARG
+        with pytest.raises(F.MoEError) as e:
+            m.set_slot_table([0, 1, 2, 3, 4, 5, 6, 8])
+        assert e.value.status == F.ERR_INVALID_ARG
+        with pytest.raises(F.MoEError) as e:
+            m.pack_experts(7, *(a[:2] for a in tiny.experts.arrays()))
+        assert e.value.status == F.ERR_INVALID_ARG
+        torch.cuda.synchronize()
+    finally:
+        m.close()
+    s = tiny.shape
+    m2 = moe_w4a16.MoELayer(s.hidden, s.inter, s.num_experts, s.top_k, num_slots=9, max_tokens=8)
+    try:
+        m2.pack_experts(0, *tiny.experts.arrays())
+        with pytest.raises(F.MoEError) as e:
+            m2.set_slot_table([0, 1, 2, 3, 4, 5, 6, 8])   # slot 8 never packed
+        assert e.value.status == F.ERR_NOT_PACKED
+        with pytest.raises(F.MoEError) as e:
+            m2.forward(gp.to_dev(synth.draw_x(1, 2, 256)), gp.to_dev(tiny.router_w))   # no table yet
+        assert e.value.status == F.ERR_INVALID_ARG
+    finally:
+        m2.close()
+
+
+def test_device_source_pack_matches_host_pack(tiny):
+    import torch
+    x = synth.draw_x(4, 6, 256)
+    m = gp.make_handle(tiny, 8)
+    s = tiny.shape
+    m2 = moe_w4a16.MoELayer(s.hidden, s.inter, s.num_experts, s.top_k, max_tokens=8)
+    try:
+        m2.pack_experts(0, *(torch.from_numpy(a).cuda() for a in tiny.experts.arrays()))
+        m2.set_slot_table(tiny.expert_to_slot)
+        o1, _ = gp.gpu_forward(m, tiny, x)
+        o2, _ = gp.gpu_forward(m2, tiny, x)
+    finally:
+        m.close()
+        m2.close()
+    assert np.array_equal(o1, o2)

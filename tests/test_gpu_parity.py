@@ -1,0 +1,66 @@
+"""CUDA path vs the CPU oracle on the seeded workloads (element-wise)."""
+import numpy as np
+import pytest
+
+from tests import gpu_parity as gp
+from w4a16_compact_expert_gb300 import moe_w4a16, synth
+
+pytestmark = pytest.mark.gpu
+
+F = moe_w4a16
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return synth.tiny_layer()
+
+
+@pytest.fixture(scope="module")
+def olmoe():
+    return synth.olmoe_decode_layer()
+
+
+@pytest.fixture(scope="module")
+def qwen():
+    return synth.qwen_partial_layer()
+
+
+@pytest.mark.parametrize("T", [4, 1, 3, 13, 37, 64, 100, 257])
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMV])
+def test_tiny(tiny, T, force):
+    x = synth.draw_x(synth.SEED_TINY, T, tiny.shape.hidden)
+    err, nflag = gp.check_full(tiny, x, flags=force, max_tokens=max(T, 8))
+    print(f"tiny T={T} rel={err:.2e} flagged={nflag}")
+
+
+@pytest.mark.parametrize("flags", [F.RESIDUAL, F.PRENORM, F.RESIDUAL | F.PRENORM])
+def test_tiny_flags(tiny, flags):
+    x = synth.draw_x(synth.SEED_TINY, 20, tiny.shape.hidden)
+    gp.check_full(tiny, x, flags=flags, max_tokens=32)
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_olmoe_decode(olmoe, T):
+    x = synth.draw_x(synth.SEED_OLMOE_DECODE, T, olmoe.shape.hidden)
+    err, nflag = gp.check_full(olmoe, x, max_tokens=2048)
+    print(f"olmoe T={T} rel={err:.2e} flagged={nflag}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_qwen_partial(qwen, T):
+    x = synth.draw_x(synth.SEED_QWEN_PARTIAL, T, qwen.shape.hidden)
+    err, nflag = gp.check_full(qwen, x, max_tokens=64)
+    print(f"qwen T={T} rel={err:.2e} flagged={nflag}")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("force", [F.FORCE_GEMV])
+def test_olmoe_prefill_sampled(variant, force):
+    layer = synth.olmoe_prefill_layer(variant)
+    seed = synth.SEED_OLMOE_PREFILL if variant == 1 else synth.SEED_OLMOE_PREFILL_SKEW
+    T = 2048
+    x = synth.draw_x(seed, T, layer.shape.hidden)
+    rows = np.random.default_rng(variant).choice(T, size=40, replace=False)
+    rows = np.concatenate([rows, [0, T - 1]])
+    err, nflag = gp.check_sampled(layer, x, rows, flags=force)
+    print(f"prefill v{variant} sampled rel={err:.2e} flagged={nflag}")

@@ -1,0 +1,66 @@
+// Internal (non-ABI) declarations shared by the host runtime and the kernels.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "layout.h"
+
+// Everything one forward needs, resolved by the host runtime.
+struct FwdCtx {
+  // problem
+  const __half* x;
+  int T;
+  const __half* router_w;
+  const float* bias;
+  uint32_t flags;
+  __half* out;
+  int H, I, E, k;
+  // experts
+  const uint8_t* pool;
+  uint64_t slot_bytes;
+  SlotLayout lay;
+  const int32_t* table;        // [E] expert -> slot, -1 absent
+  // routing workspaces
+  int ksplit;                  // K split of the router logits
+  float* logit_part;           // [ksplit][T][E]
+  float* ss_part;              // [ksplit][T] partial sum of squares (PRENORM)
+  float* rnorm;                // [T] 1/rms (PRENORM) else unused
+  int32_t* ids;                // [T*k]
+  float* topw;                 // [T*k]
+  int32_t* offsets;            // [E+1]
+  int32_t* sorted;             // [T*k] sorted row -> flat pair
+  int32_t* p2r;                // [T*k] flat pair -> sorted row
+  int32_t* act_expert;         // [E] active (routed and resident) experts, ascending
+  int32_t* act_slot;           // [E]
+  int32_t* act_start;          // [E] first sorted row of the group
+  int32_t* act_count;          // [E] rows of the group
+  int32_t* act_tile;           // [E+1] prefix of token tiles per active expert
+  int32_t* n_active;           // [1]
+  int tile_tokens;             // token tile of the grouped GEMM
+  // expert workspaces
+  __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
+  float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
+  unsigned* route_counter;     // [1] arrival counter (self-resetting)
+  unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
+  DevStatus* status;
+  int num_sms;
+  int max_active;              // upper bound of active experts: min(E, T*k)
+};
+
+// repack.cu
+cudaError_t launch_repack_matrix(const uint8_t* q, const uint16_t* s, uint8_t* slot_base,
+                                 const MatLayout& m, cudaStream_t st);
+
+// route.cu
+cudaError_t launch_route(const FwdCtx& c, bool fused, cudaStream_t st);
+
+// gemv.cu
+cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st);
+
+// gemm_tc.cu
+cudaError_t launch_gemm_experts(const FwdCtx& c, cudaStream_t st);
+
+// route: the largest T handled by the fused single-launch router
+#define ROUTE_FUSED_MAX_T 64

@@ -1,0 +1,181 @@
+"""Thin ctypes binding of the C ABI in include/moe_w4a16.h.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+PyTorch supplies device memory and the current stream.  The library is
+loaded on first use; if it is missing (not built) the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_w4a16.so")
+
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_PACKED, ERR_NOT_RESIDENT, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
+STATUS_NAMES = ["OK", "ERR_INVALID_ARG", "ERR_CUDA", "ERR_OOM", "ERR_NOT_PACKED", "ERR_NOT_RESIDENT",
+                "ERR_TIMEOUT", "ERR_UNSUPPORTED"]
+RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM = 1, 2, 4, 8
+
+EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
+            "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
+            "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens"]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("device", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES[status] if 0 <= status < 8 else status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load (once) and return the CUDA library; raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, u32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int64)
+    lib.moe_w4a16_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(vp)]
+    lib.moe_w4a16_destroy.argtypes = [vp]
+    lib.moe_w4a16_pack_experts.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.moe_w4a16_set_slot_table.argtypes = [vp, vp, vp]
+    lib.moe_w4a16_forward.argtypes = [vp, vp, i32, vp, vp, u32, vp, vp, vp, vp, vp, vp]
+    lib.moe_w4a16_forward_host.argtypes = [vp, vp, i32, vp, vp, u32, vp, vp]
+    lib.moe_w4a16_get_status.argtypes = [vp, i64p]
+    lib.moe_w4a16_last_error.argtypes = [vp]
+    lib.moe_w4a16_last_error.restype = ctypes.c_char_p
+    lib.moe_w4a16_slot_bytes.argtypes = [vp]
+    lib.moe_w4a16_slot_bytes.restype = ctypes.c_size_t
+    lib.moe_w4a16_get_gemv_max_tokens.argtypes = [vp]
+    lib.moe_w4a16_get_gemv_max_tokens.restype = i32
+    lib.moe_w4a16_set_gemv_max_tokens.argtypes = [vp, i32]
+    _lib = lib
+    return lib
+
+
+def _ptr(a) -> Optional[int]:
+    """Device or host address of a torch tensor / numpy array (None -> NULL)."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("numpy array must be C-contiguous")
+        return a.ctypes.data
+    if not a.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return a.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class MoELayer:
+    """One W4A16 routed-expert MoE layer on one GPU (a library handle)."""
+
+    def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, num_slots: Optional[int] = None,
+                 max_tokens: int = 2048, device: int = 0):
+        self.lib = load_library()
+        self.cfg = Config(hidden, inter, num_experts, top_k, num_experts if num_slots is None else num_slots,
+                          max_tokens, device)
+        h = ctypes.c_void_p()
+        st = self.lib.moe_w4a16_create(ctypes.byref(self.cfg), ctypes.byref(h))
+        if st != OK:
+            raise MoEError(st, self.lib.moe_w4a16_last_error(None).decode())
+        self.h = h
+        self.device = device
+
+    # -- helpers
+    def _check(self, st: int):
+        if st != OK:
+            raise MoEError(st, self.lib.moe_w4a16_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.moe_w4a16_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:   # noqa: BLE001 - interpreter shutdown
+            pass
+
+    @property
+    def slot_bytes(self) -> int:
+        return self.lib.moe_w4a16_slot_bytes(self.h)
+
+    @property
+    def gemv_max_tokens(self) -> int:
+        return self.lib.moe_w4a16_get_gemv_max_tokens(self.h)
+
+    @gemv_max_tokens.setter
+    def gemv_max_tokens(self, v: int):
+        self._check(self.lib.moe_w4a16_set_gemv_max_tokens(self.h, int(v)))
+
+    # -- API
+    def pack_experts(self, slot0: int, gate_q, gate_s, up_q, up_s, down_q, down_s, stream=None):
+        """Canonical qpacked arrays (numpy or torch, host or device), leading axis = expert."""
+        n = int(gate_q.shape[0])
+        self._check(self.lib.moe_w4a16_pack_experts(self.h, slot0, n, _ptr(gate_q), _ptr(gate_s), _ptr(up_q),
+                                                    _ptr(up_s), _ptr(down_q), _ptr(down_s), _stream(stream)))
+
+    def set_slot_table(self, expert_to_slot, stream=None):
+        t = np.ascontiguousarray(np.asarray(expert_to_slot, dtype=np.int32))
+        self._check(self.lib.moe_w4a16_set_slot_table(self.h, t.ctypes.data, _stream(stream)))
+
+    def forward(self, x, router_w, bias=None, flags: int = 0, out=None, debug: bool = False, stream=None):
+        """x: cuda fp16 [T, H].  Returns out (and a dict of routing tensors if debug)."""
+        import torch
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty_like(x)
+        dbg = {}
+        if debug:
+            k, E = self.cfg.top_k, self.cfg.num_experts
+            dev = x.device
+            dbg = {"ids": torch.empty(T, k, dtype=torch.int32, device=dev),
+                   "weights": torch.empty(T, k, dtype=torch.float32, device=dev),
+                   "sorted_pairs": torch.empty(T * k, dtype=torch.int32, device=dev),
+                   "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev)}
+        self._check(self.lib.moe_w4a16_forward(
+            self.h, _ptr(x), T, _ptr(router_w), _ptr(bias), flags, _ptr(out), _ptr(dbg.get("ids")),
+            _ptr(dbg.get("weights")), _ptr(dbg.get("sorted_pairs")), _ptr(dbg.get("offsets")), _stream(stream)))
+        return (out, dbg) if debug else out
+
+    def forward_raw(self, x_ptr: int, T: int, router_w_ptr: int, bias_ptr, flags: int, out_ptr: int, stream_ptr):
+        """Pointer-level forward (no torch objects), for timing loops."""
+        return self.lib.moe_w4a16_forward(self.h, x_ptr, T, router_w_ptr, bias_ptr, flags, out_ptr,
+                                          None, None, None, None, stream_ptr)
+
+    def forward_host(self, x_host, router_w, bias=None, flags: int = 0, out_host=None, stream=None):
+        """x_host: host fp16 [T, H] (numpy or pinned torch).  Synchronous."""
+        T = int(x_host.shape[0])
+        if out_host is None:
+            out_host = np.empty_like(x_host)
+        self._check(self.lib.moe_w4a16_forward_host(self.h, _ptr(x_host), T, _ptr(router_w), _ptr(bias), flags,
+                                                    _ptr(out_host), _stream(stream)))
+        return out_host
+
+    def get_status(self):
+        """(status code, miss count); synchronises the device and clears the word."""
+        miss = ctypes.c_int64(0)
+        st = self.lib.moe_w4a16_get_status(self.h, ctypes.byref(miss))
+        return st, miss.value
