@@ -168,6 +168,16 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t
  * the message of the last failed create. */
 MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
 
+/* Profiling aid.  With events != NULL (an array of 5 cudaEvent_t created by
+ * the caller with timing enabled), every later forward on this handle records
+ * them on its stream at the stage boundaries: [0] before routing, [1] after
+ * routing, [2] after the gate/up kernel, [3] after the down kernel, [4] after
+ * the combine ([4] == [3] in the decode regime, whose down kernel also does
+ * the combine).  While the stream is being captured they are recorded as
+ * external event nodes of the graph.  NULL turns recording off.  The handle
+ * keeps the five pointers, not the array. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_set_stage_events(moe_w4a16_handle* h, void* const* events);
+
 /* Bytes of one slot row in the pool (compact weights + scales + padding). */
 MOE_W4A16_API size_t moe_w4a16_slot_bytes(const moe_w4a16_handle* h);
 

@@ -9,6 +9,7 @@
 // separate objects.
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -45,6 +46,7 @@ struct moe_w4a16_handle {
   size_t stage_bytes = 0;
   __half* x_dev = nullptr;           // forward_host staging
   __half* out_dev = nullptr;
+  StageEvents events{};
   std::vector<void*> allocs;
   std::string err;
 };
@@ -110,6 +112,35 @@ int fused_ksplit(int H) {
 
 }  // namespace
 
+cudaError_t opt_in_smem(const void* func, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  struct Entry {
+    const void* f;
+    int dev;
+    size_t v;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : done)
+    if (x.f == func && x.dev == dev && x.v >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.push_back({func, dev, bytes});
+  return e;
+}
+
+cudaError_t record_stage(const StageEvents& se, int i, cudaStream_t st) {
+  if (!se.on) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(se.ev[i], st, cudaEventRecordExternal);
+  return cudaEventRecord(se.ev[i], st);
+}
+
 extern "C" {
 
 moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle** out) {
@@ -140,6 +171,12 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
              c.num_slots, c.max_tokens, c.device);
     g_create_err = buf;
     return MOE_W4A16_ERR_INVALID_ARG;
+  }
+  if (gemv_smem_gateup(c.hidden, c.inter, 8) > 220 * 1024 || gemv_smem_down(c.hidden, c.inter, 8) > 220 * 1024) {
+    snprintf(buf, sizeof buf, "hidden %d / inter %d too large for the decode kernels' shared memory", c.hidden,
+             c.inter);
+    g_create_err = buf;
+    return MOE_W4A16_ERR_UNSUPPORTED;
   }
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || c.device >= ndev) {
@@ -206,6 +243,20 @@ moe_w4a16_status moe_w4a16_destroy(moe_w4a16_handle* h) {
     free_all(h);
   }
   delete h;
+  return MOE_W4A16_OK;
+}
+
+moe_w4a16_status moe_w4a16_set_stage_events(moe_w4a16_handle* h, void* const* events) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  if (!events) {
+    h->events.on = false;
+    return MOE_W4A16_OK;
+  }
+  for (int i = 0; i < 5; ++i) {
+    if (!events[i]) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "NULL stage event");
+    h->events.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  h->events.on = true;
   return MOE_W4A16_OK;
 }
 
@@ -351,15 +402,17 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.out = static_cast<__half*>(out);
   const bool gemm = (flags & MOE_W4A16_FORCE_GEMM) || (!(flags & MOE_W4A16_FORCE_GEMV) && T > h->gemv_max_tokens);
   const bool fused_route = T <= ROUTE_FUSED_MAX_T;
-  c.ksplit = fused_route ? h->ksplit_fused : 1;
+  c.ksplit = 1;
   c.tile_tokens = 128;
   int ma = c.E;
   if ((long long)T * c.k < ma) ma = T * c.k;
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
   c.max_active = ma;
-  cudaError_t e = launch_route(c, fused_route, st);
+  cudaError_t e = record_stage(h->events, 0, st);
+  if (e == cudaSuccess) e = launch_route(c, fused_route, st);
+  if (e == cudaSuccess) e = record_stage(h->events, 1, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
-  e = gemm ? launch_gemm_experts(c, st) : launch_gemv_experts(c, st);
+  e = gemm ? launch_gemm_experts(c, st, h->events) : launch_gemv_experts(c, st, h->events);
   if (e == cudaErrorNotSupported) return fail(h, MOE_W4A16_ERR_UNSUPPORTED, "grouped GEMM path not available");
   if (e != cudaSuccess) return cuda_fail(h, e, "expert launch");
   const size_t P = (size_t)T * c.k;

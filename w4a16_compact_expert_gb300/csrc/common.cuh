@@ -61,14 +61,91 @@ DEV_INLINE float warp_sum(float v) {
 
 DEV_INLINE float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-// Pointer to the 16-byte chunk (kc, rt, lane) of a matrix in a slot row.
-DEV_INLINE const uint4* chunk_ptr(const uint8_t* slot_base, const MatLayout& m, int kc, int rt, int lane) {
-  const uint4* q = reinterpret_cast<const uint4*>(slot_base + m.q_off);
-  return q + ((size_t)kc * (m.rows / 16) + rt) * 32 + lane;
+// Start of 16-row tile rt of a matrix in a slot row (layout.h).
+DEV_INLINE const uint8_t* tile_ptr(const uint8_t* slot_base, const MatLayout& m, int rt) {
+  return slot_base + m.off + (size_t)rt * m.tile_bytes;
 }
 
-DEV_INLINE const __half* scale_ptr(const uint8_t* slot_base, const MatLayout& m) {
-  return reinterpret_cast<const __half*>(slot_base + m.s_off);
+// ---------------------------------------------------------------- mbarrier
+DEV_INLINE uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+DEV_INLINE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+DEV_INLINE void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+DEV_INLINE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+DEV_INLINE void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+DEV_INLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~2^31 SM cycles (about
+// one second), records STATUS_TIMEOUT and returns false.  No wait in this
+// library is unbounded.
+#define MOE_WAIT_CYCLES (1ll << 31)
+DEV_INLINE bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, DevStatus* st) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// 1-D bulk async copy global -> shared (TMA, no tensor map), completing on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+DEV_INLINE void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------- programmatic dependent launch
+// wait: block until the preceding grid in the stream completed and its
+// memory is visible (no-op when not launched with the PDL attribute).
+DEV_INLINE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// allow the next grid in the stream to start launching.
+DEV_INLINE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------------ cluster
+DEV_INLINE uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+DEV_INLINE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of `p` (in this CTA's smem) mapped into CTA `rank`.
+DEV_INLINE uint32_t map_to_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+DEV_INLINE void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // 128-bit streaming load that does not allocate in L1 (weights are read once).

@@ -1,12 +1,12 @@
 // Decode regime: grouped split-K GEMV over compact int4 experts.
 //
-// Weights are streamed once from HBM with 128-bit loads in the internal
-// fragment order (layout.h), dequantised in registers (never written back
-// anywhere), and multiplied on the tensor cores with FP16 operands and FP32
-// accumulation (Horizon RunMap landing page, "08 / Precision & quality":
-// compact weights converted in-kernel, FP32 accumulation stages, explicit
-// rounding).  Explicit FP16 rounding points: h = SiLU(g) * u before the down
-// projection, and the final output.
+// Each CTA fetches its weight tiles (compact int4 + FP16 scales, layout.h)
+// with 1-D bulk async copies (TMA) into shared memory, dequantises them in
+// registers (nothing expanded is ever written anywhere) and multiplies on the
+// tensor cores with FP16 operands and FP32 accumulation (Horizon RunMap
+// landing page, "08 / Precision & quality": compact weights converted
+// in-kernel, FP32 accumulation stages, explicit rounding).  Explicit FP16
+// rounding points: h = SiLU(g) * u before the down projection, and the output.
 //
 //   gate/up : CTA = (16-row tile of I, active expert); 8 warps split K; the
 //             SiLU*up epilogue writes h [sorted row][I] in FP16.
@@ -15,113 +15,114 @@
 //             CTA to finish a 32-row block (arrival counter, no waiting)
 //             gathers out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] for that block,
 //             summing in rank order j (deterministic, no atomics on data).
+// Launch chain: route -> gate/up -> down with programmatic dependent launch.
+// The down CTAs start fetching their weight tiles as soon as they are
+// resident (routing is complete by then) and wait for h only to multiply.
 #include "internal.h"
 
 namespace {
 
-constexpr int kTok = 8;           // tokens per pass (one MMA n-tile)
-constexpr int kGroup = 4;         // 64-wide K chunks a warp holds in flight
+constexpr int kTok = 8;   // tokens per pass (one MMA n-tile)
 
-struct ChunkRegs {
-  uint4 q[kGroup];
-  __half2 s_lo[kGroup], s_hi[kGroup];
-};
-
-DEV_INLINE void load_chunks(ChunkRegs& r, const uint8_t* base, const MatLayout& m, int rt, int lane,
-                            int kc0, int kstride, int nkc) {
-  const int g = lane >> 2;
-  const __half* s = scale_ptr(base, m);
-#pragma unroll
-  for (int i = 0; i < kGroup; ++i) {
-    const int kc = kc0 + i * kstride;
-    if (kc < nkc) {
-      r.q[i] = ld_stream(chunk_ptr(base, m, kc, rt, lane));
-      const int b = kc >> 2;   // 256-wide scale block of this 64-wide chunk
-      r.s_lo[i] = __half2half2(s[(size_t)b * m.rows + rt * 16 + g]);
-      r.s_hi[i] = __half2half2(s[(size_t)b * m.rows + rt * 16 + g + 8]);
-    }
-  }
+DEV_INLINE uint32_t lds_b32_or0(const __half* p, bool valid) {
+  return valid ? *reinterpret_cast<const uint32_t*>(p) : 0u;
 }
 
-// acc += W[rt rows, chunks] * B, B read from an smem tile [kTok][stride] of FP16.
-DEV_INLINE void mma_chunks(float (&acc)[4], const ChunkRegs& r, const __half* bs, int stride, int lane,
-                           int kc0, int kstride, int nkc) {
+// acc[m] += tile[m] rows x B over chunks kc = kc0, kc0 + kstride, ... (< nkc).
+// B rows live in smem [np][stride] FP16; rows >= np read as zero.
+template <int NMAT>
+DEV_INLINE void mma_tiles(float (&acc)[2][4], const uint8_t* const (&tile)[2], uint32_t scale_bytes,
+                          const __half* bs, int stride, int np, int lane, int kc0, int kstride, int nkc) {
   const int g = lane >> 2, c = lane & 3;
+  const bool brow = g < np;
+  for (int kc = kc0; kc < nkc; kc += kstride) {
+    uint4 q[NMAT];
+    __half2 slo[NMAT], shi[NMAT];
 #pragma unroll
-  for (int i = 0; i < kGroup; ++i) {
-    const int kc = kc0 + i * kstride;
-    if (kc < nkc) {
-      const uint32_t words[4] = {r.q[i].x, r.q[i].y, r.q[i].z, r.q[i].w};
+    for (int m = 0; m < NMAT; ++m) {
+      q[m] = *reinterpret_cast<const uint4*>(tile[m] + scale_bytes + ((size_t)kc * 32 + lane) * 16);
+      const __half* sc = reinterpret_cast<const __half*>(tile[m]) + (kc >> 2) * 16;
+      slo[m] = __half2half2(sc[g]);
+      shi[m] = __half2half2(sc[g + 8]);
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 4; ++j) {
+      const __half* bp = bs + g * stride + kc * 64 + j * 16 + 2 * c;
+      const uint32_t b0 = lds_b32_or0(bp, brow), b1 = lds_b32_or0(bp + 8, brow);
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        const uint32_t w = j == 0 ? q[m].x : j == 1 ? q[m].y : j == 2 ? q[m].z : q[m].w;
         uint32_t a[4];
-        dequant_word(words[j], r.s_lo[i], r.s_hi[i], a);
-        const int k0 = kc * 64 + j * 16;
-        const __half* brow = bs + g * stride + k0 + 2 * c;
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(brow);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(brow + 8);
-        mma_16816(acc, a, b0, b1);
+        dequant_word(w, slo[m], shi[m], a);
+        mma_16816(acc[m], a, b0, b1);
       }
     }
   }
 }
 
-// Stage up to kTok FP16 rows (gathered by row index) into smem [kTok][stride].
+// Stage `nrows` FP16 rows (gathered by row index) into smem [*][stride].
 DEV_INLINE void stage_rows(__half* dst, int stride, int K, const __half* src, const int32_t* rows, int nrows) {
   const int vec_per_row = K / 8;
-  for (int i = threadIdx.x; i < kTok * vec_per_row; i += blockDim.x) {
+  for (int i = threadIdx.x; i < nrows * vec_per_row; i += blockDim.x) {
     const int r = i / vec_per_row, v = i % vec_per_row;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (r < nrows) val = __ldg(reinterpret_cast<const uint4*>(src + (size_t)rows[r] * K) + v);
-    *(reinterpret_cast<uint4*>(dst + r * stride) + v) = val;
+    *(reinterpret_cast<uint4*>(dst + r * stride) + v) =
+        __ldg(reinterpret_cast<const uint4*>(src + (size_t)rows[r] * K) + v);
   }
 }
 
-__global__ void __launch_bounds__(256) gemv_gateup_kernel(FwdCtx c) {
+__global__ void __launch_bounds__(256) gemv_gateup_kernel(FwdCtx c, int xrows) {
+  pdl_wait();      // routing results of the preceding grid
+  pdl_trigger();
   const int u = blockIdx.y;
   if (u >= *c.n_active) return;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_tok[kTok];
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, cc = lane & 3;
   const int rt = blockIdx.x;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, cc = lane & 3;
   const int slot = c.act_slot[u], start = c.act_start[u], cnt = c.act_count[u];
   const uint8_t* base = c.pool + (size_t)slot * c.slot_bytes;
-  const int H = c.H, I = c.I, nkc = H / 64;
-  const int stride = H + 8;
-  __half* xs = reinterpret_cast<__half*>(smem);
-  float* red = reinterpret_cast<float*>(smem + (size_t)kTok * stride * sizeof(__half));  // [8][2][16][8]
-  __shared__ int s_tok[kTok];
+  const MatLayout& LG = c.lay.gate;
+  const int H = c.H, I = c.I, nkc = H / 64, stride = H + 8;
+  const uint32_t TS = LG.tile_bytes;
+  const uint8_t* const tiles[2] = {smem, smem + TS};
+  __half* xs = reinterpret_cast<__half*>(smem + 2 * (size_t)TS);
+  float* red = reinterpret_cast<float*>(smem + 2 * (size_t)TS + (size_t)xrows * stride * sizeof(__half));
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar, 2 * TS);
+    bulk_g2s(smem, tile_ptr(base, LG, rt), TS, &bar);
+    bulk_g2s(smem + TS, tile_ptr(base, c.lay.up, rt), TS, &bar);
+  }
   for (int p0 = 0; p0 < cnt; p0 += kTok) {
     const int np = min(kTok, cnt - p0);
-    ChunkRegs rg, ru;
-    load_chunks(rg, base, c.lay.gate, rt, lane, w, 8, nkc);
-    load_chunks(ru, base, c.lay.up, rt, lane, w, 8, nkc);
-    __syncthreads();   // previous pass is done with xs / red / s_tok
-    if (threadIdx.x < kTok) s_tok[threadIdx.x] = threadIdx.x < np ? c.sorted[start + p0 + threadIdx.x] / c.k : 0;
+    __syncthreads();   // previous pass done with xs / red / s_tok; barrier init visible
+    if (tid < np) s_tok[tid] = c.sorted[start + p0 + tid] / c.k;
     __syncthreads();
     stage_rows(xs, stride, H, c.x, s_tok, np);
-    __syncthreads();
-    float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_chunks(ag, rg, xs, stride, lane, w, 8, nkc);
-    mma_chunks(au, ru, xs, stride, lane, w, 8, nkc);
-    for (int kc0 = w + 8 * kGroup; kc0 < nkc; kc0 += 8 * kGroup) {
-      load_chunks(rg, base, c.lay.gate, rt, lane, kc0, 8, nkc);
-      load_chunks(ru, base, c.lay.up, rt, lane, kc0, 8, nkc);
-      mma_chunks(ag, rg, xs, stride, lane, kc0, 8, nkc);
-      mma_chunks(au, ru, xs, stride, lane, kc0, 8, nkc);
+    if (p0 == 0) {
+      if (tid == 0) s_ok = 1;
+      __syncthreads();
+      if (!mbar_wait_bounded(&bar, 0, c.status)) s_ok = 0;
     }
+    __syncthreads();
+    if (!s_ok) return;   // timed out: give up (the status word records it)
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    mma_tiles<2>(acc, tiles, LG.scale_bytes, xs, stride, np, lane, w, 8, nkc);
     // accumulator (row g / g+8, token 2cc / 2cc+1) -> red[w][mat][row][tok]
     float* rw = red + w * 2 * 16 * kTok;
-    rw[(0 * 16 + g) * kTok + 2 * cc] = ag[0];
-    rw[(0 * 16 + g) * kTok + 2 * cc + 1] = ag[1];
-    rw[(0 * 16 + g + 8) * kTok + 2 * cc] = ag[2];
-    rw[(0 * 16 + g + 8) * kTok + 2 * cc + 1] = ag[3];
-    rw[(1 * 16 + g) * kTok + 2 * cc] = au[0];
-    rw[(1 * 16 + g) * kTok + 2 * cc + 1] = au[1];
-    rw[(1 * 16 + g + 8) * kTok + 2 * cc] = au[2];
-    rw[(1 * 16 + g + 8) * kTok + 2 * cc + 1] = au[3];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      rw[(m * 16 + g) * kTok + 2 * cc] = acc[m][0];
+      rw[(m * 16 + g) * kTok + 2 * cc + 1] = acc[m][1];
+      rw[(m * 16 + g + 8) * kTok + 2 * cc] = acc[m][2];
+      rw[(m * 16 + g + 8) * kTok + 2 * cc + 1] = acc[m][3];
+    }
     __syncthreads();
-    if (threadIdx.x < 16 * kTok) {
-      const int row = threadIdx.x / kTok, tok = threadIdx.x % kTok;
+    if (tid < 16 * kTok) {
+      const int row = tid / kTok, tok = tid % kTok;
       if (tok < np) {
         float gs = 0.f, us = 0.f;
 #pragma unroll
@@ -140,51 +141,72 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(FwdCtx c) {
   }
 }
 
-__global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c) {
-  const int u = blockIdx.y, hb = blockIdx.x;
-  const int nact = *c.n_active;
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c, int hrows) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_rows[kTok];
+  __shared__ int s_ok;
   __shared__ unsigned s_last;
-  const int H = c.H, I = c.I;
+  const int u = blockIdx.y, hb = blockIdx.x;
   const int tid = threadIdx.x;
-  if (u < nact) {
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, cc = lane & 3;
-    const int rt = hb * 2 + (w >> 2), wk = w & 3;
-    const int slot = c.act_slot[u], start = c.act_start[u], cnt = c.act_count[u];
-    const uint8_t* base = c.pool + (size_t)slot * c.slot_bytes;
-    const int nkc = I / 64;
-    const int stride = I + 8;
-    __half* hs = reinterpret_cast<__half*>(smem);
-    float* red = reinterpret_cast<float*>(smem + (size_t)kTok * stride * sizeof(__half));  // [8][16][8]
-    __shared__ int s_rows[kTok];
+  const int H = c.H, I = c.I;
+  const MatLayout& LD = c.lay.down;
+  const uint32_t TS = LD.tile_bytes;
+  // Routing finished before the gate/up grid let this grid launch: read it
+  // from L2 and start fetching this CTA's weight tiles before waiting for h.
+  const int nact = __ldcg(c.n_active);
+  const bool active = u < nact;
+  int start = 0, cnt = 0;
+  if (active) {
+    const int slot = __ldcg(&c.act_slot[u]);
+    start = __ldcg(&c.act_start[u]);
+    cnt = __ldcg(&c.act_count[u]);
+    if (tid == 0) {
+      const uint8_t* base = c.pool + (size_t)slot * c.slot_bytes;
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      mbar_expect_tx(&bar, 2 * TS);
+      bulk_g2s(smem, tile_ptr(base, LD, 2 * hb), TS, &bar);
+      bulk_g2s(smem + TS, tile_ptr(base, LD, 2 * hb + 1), TS, &bar);
+    }
+  }
+  pdl_wait();      // h of the gate/up grid
+  pdl_trigger();
+  if (active) {
+    const int w = tid >> 5, lane = tid & 31, g = lane >> 2, cc = lane & 3;
+    const int half_sel = w >> 2, wk = w & 3;
+    const int nkc = I / 64, stride = I + 8;
+    const uint8_t* const tiles[2] = {smem + (size_t)half_sel * TS, nullptr};
+    __half* hs = reinterpret_cast<__half*>(smem + 2 * (size_t)TS);
+    float* red = reinterpret_cast<float*>(smem + 2 * (size_t)TS + (size_t)hrows * stride * sizeof(__half));
     for (int p0 = 0; p0 < cnt; p0 += kTok) {
       const int np = min(kTok, cnt - p0);
-      ChunkRegs rd;
-      load_chunks(rd, base, c.lay.down, rt, lane, wk, 4, nkc);
       __syncthreads();
-      if (tid < kTok) s_rows[tid] = start + p0 + (tid < np ? tid : 0);
+      if (tid < np) s_rows[tid] = start + p0 + tid;
       __syncthreads();
       stage_rows(hs, stride, I, c.hbuf, s_rows, np);
-      __syncthreads();
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_chunks(acc, rd, hs, stride, lane, wk, 4, nkc);
-      for (int kc0 = wk + 4 * kGroup; kc0 < nkc; kc0 += 4 * kGroup) {
-        load_chunks(rd, base, c.lay.down, rt, lane, kc0, 4, nkc);
-        mma_chunks(acc, rd, hs, stride, lane, kc0, 4, nkc);
+      if (p0 == 0) {
+        if (tid == 0) s_ok = 1;
+        __syncthreads();
+        if (!mbar_wait_bounded(&bar, 0, c.status)) s_ok = 0;
       }
+      __syncthreads();
+      if (!s_ok) break;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      mma_tiles<1>(acc, tiles, LD.scale_bytes, hs, stride, np, lane, wk, 4, nkc);
       float* rw = red + w * 16 * kTok;
-      rw[g * kTok + 2 * cc] = acc[0];
-      rw[g * kTok + 2 * cc + 1] = acc[1];
-      rw[(g + 8) * kTok + 2 * cc] = acc[2];
-      rw[(g + 8) * kTok + 2 * cc + 1] = acc[3];
+      rw[g * kTok + 2 * cc] = acc[0][0];
+      rw[g * kTok + 2 * cc + 1] = acc[0][1];
+      rw[(g + 8) * kTok + 2 * cc] = acc[0][2];
+      rw[(g + 8) * kTok + 2 * cc + 1] = acc[0][3];
       __syncthreads();
       {   // 256 threads = 32 rows x 8 tokens
         const int row = tid / kTok, tok = tid % kTok;
-        const int half_sel = row >> 4, r16 = row & 15;
+        const int hsel = row >> 4, r16 = row & 15;
         if (tok < np) {
           float y = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < 4; ++ww) y += red[(half_sel * 4 + ww) * 16 * kTok + r16 * kTok + tok];
+          for (int ww = 0; ww < 4; ++ww) y += red[(hsel * 4 + ww) * 16 * kTok + r16 * kTok + tok];
           const int pair = c.sorted[start + p0 + tok];
           c.ybuf[(size_t)pair * H + hb * 32 + row] = y;
         }
@@ -195,7 +217,7 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c) {
   __syncthreads();
   if (tid == 0) {
     unsigned last = 0;
-    if (u < nact) last = (atomicAdd(&c.down_counters[hb], 1u) == (unsigned)nact - 1u) ? 1u : 0u;
+    if (active) last = (atomicAdd(&c.down_counters[hb], 1u) == (unsigned)nact - 1u) ? 1u : 0u;
     s_last = last;
   }
   __syncthreads();
@@ -217,14 +239,27 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c) {
 
 }  // namespace
 
-cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st) {
-  const size_t smem_gu = (size_t)kTok * (c.H + 8) * sizeof(__half) + 8 * 2 * 16 * kTok * sizeof(float);
-  const size_t smem_dn = (size_t)kTok * (c.I + 8) * sizeof(__half) + 8 * 16 * kTok * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(gemv_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
+size_t gemv_smem_gateup(int H, int I, int rows) {
+  const SlotLayout L = moe_slot_layout(H, I);
+  return 2 * (size_t)L.gate.tile_bytes + (size_t)rows * (H + 8) * sizeof(__half) + 8 * 2 * 16 * kTok * sizeof(float);
+}
+
+size_t gemv_smem_down(int H, int I, int rows) {
+  const SlotLayout L = moe_slot_layout(H, I);
+  return 2 * (size_t)L.down.tile_bytes + (size_t)rows * (I + 8) * sizeof(__half) + 8 * 16 * kTok * sizeof(float);
+}
+
+cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
+  const int rows = c.T < kTok ? c.T : kTok;
+  const size_t smem_gu = gemv_smem_gateup(c.H, c.I, rows);
+  const size_t smem_dn = gemv_smem_down(c.H, c.I, rows);
+  cudaError_t e = opt_in_smem((const void*)gemv_gateup_kernel, smem_gu);
+  if (e == cudaSuccess) e = opt_in_smem((const void*)gemv_down_kernel, smem_dn);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemv_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
-  if (e != cudaSuccess) return e;
-  gemv_gateup_kernel<<<dim3(c.I / 16, c.max_active), 256, smem_gu, st>>>(c);
-  gemv_down_kernel<<<dim3(c.H / 32, c.max_active), 256, smem_dn, st>>>(c);
-  return cudaGetLastError();
+  e = launch_pdl(gemv_gateup_kernel, dim3(c.I / 16, c.max_active), dim3(256), smem_gu, st, 1, c, rows);
+  if (e == cudaSuccess) e = record_stage(se, 2, st);
+  if (e == cudaSuccess) e = launch_pdl(gemv_down_kernel, dim3(c.H / 32, c.max_active), dim3(256), smem_dn, st, 1, c, rows);
+  if (e == cudaSuccess) e = record_stage(se, 3, st);
+  if (e == cudaSuccess) e = record_stage(se, 4, st);
+  return e;
 }

@@ -56,11 +56,54 @@ cudaError_t launch_repack_matrix(const uint8_t* q, const uint16_t* s, uint8_t* s
 // route.cu
 cudaError_t launch_route(const FwdCtx& c, bool fused, cudaStream_t st);
 
-// gemv.cu
-cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st);
+// Records the optional stage event `i` of a forward (no-op when unset).
+struct StageEvents {
+  cudaEvent_t ev[5];
+  bool on;
+};
+cudaError_t record_stage(const StageEvents& se, int i, cudaStream_t st);
 
-// gemm_tc.cu
-cudaError_t launch_gemm_experts(const FwdCtx& c, cudaStream_t st);
+// gemv.cu: decode regime (gate/up kernel, then down kernel with the combine)
+cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
 
-// route: the largest T handled by the fused single-launch router
+// gemm_tc.cu: prefill regime (gate/up GEMM, down GEMM, combine)
+cudaError_t launch_gemm_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
+
+// route: the largest T handled by the single-launch cluster router
 #define ROUTE_FUSED_MAX_T 64
+
+// gemv.cu: dynamic shared memory of the decode kernels for `rows` staged tokens.
+size_t gemv_smem_gateup(int H, int I, int rows);
+size_t gemv_smem_down(int H, int I, int rows);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` (once per
+// device and value; thread-safe).
+cudaError_t opt_in_smem(const void* func, size_t bytes);
+
+// Launch with programmatic dependent launch allowed (the kernel must call
+// griddepcontrol.wait before consuming the preceding grid's output) and an
+// optional 1-D thread-block cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}

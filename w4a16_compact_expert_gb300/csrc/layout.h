@@ -1,20 +1,19 @@
 // Kernel-internal compact layout of one expert slot (host + device).
 //
 // Each matrix W [R][K] (R output rows, K reduction) keeps 4 bits per weight.
-// Packed int4: 16-byte chunks, one per (kc, rt, lane) with kc = K/64 chunk,
-// rt = 16-row tile, lane = 0..31, at chunk index (kc * (R/16) + rt) * 32 + lane.
-// Word j (0..3) of a chunk covers K values kc*64 + j*16 .. +15 of rows
-// rt*16 + g and rt*16 + g + 8 (g = lane/4, c = lane%4): exactly the eight
-// values one lane holds in the A operand of a 16x8x16 MMA step,
+// It is stored as R/16 row tiles; a tile is one contiguous block of
+//   [FP16 scales: nb x 16, block-major]  then  [packed int4: nkc x 32 x 16 B]
+// (nb = ceil(K/256), nkc = K/64), so a kernel fetches a whole tile with a
+// single bulk copy.  The 16-byte chunk (kc, lane) of a tile covers K values
+// kc*64 .. kc*64+63 of rows g and g + 8 of the tile (g = lane/4, c = lane%4);
+// its word j (0..3) holds the eight values one lane owns in the A operand of
+// the 16x8x16 MMA step at K offset kc*64 + j*16:
 //   a0,a1 = (row g,   k 2c, 2c+1)   a2,a3 = (row g+8, k 2c, 2c+1)
 //   a4,a5 = (row g,   k 2c+8, +9)   a6,a7 = (row g+8, k 2c+8, +9)
-// stored as offset-binary nibbles u = q + 8 at nibble positions
+// as offset-binary nibbles u = q + 8 at nibble positions
 //   a0->0, a2->1, a4->2, a6->3, a1->4, a3->5, a5->6, a7->7
 // so that masking with 0x000F000F / 0x00F000F0 (after a shift by 0 or 8)
 // yields the half2 pairs (a0,a1), (a2,a3), (a4,a5), (a6,a7).
-// For a fixed kc, consecutive row tiles are contiguous, so a block of rows
-// for one 64-wide K step is one contiguous range (bulk-copy friendly).
-// Scales: FP16 [nb][R] (block-major), nb = ceil(K/256).
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -23,16 +22,17 @@
 #define MOE_REGION_ALIGN 256
 
 struct MatLayout {
-  uint32_t rows;     // R
-  uint32_t k;        // K
-  uint32_t nb;       // ceil(K / 256)
-  uint64_t q_off;    // byte offset of packed int4 within the slot
-  uint64_t s_off;    // byte offset of FP16 scales within the slot
+  uint32_t rows;        // R
+  uint32_t k;           // K
+  uint32_t nb;          // ceil(K / 256)
+  uint32_t tile_bytes;  // nb * 32 + 8 * K  (one 16-row tile incl. its scales)
+  uint32_t scale_bytes; // nb * 32
+  uint64_t off;         // byte offset of the matrix within the slot
 };
 
 struct SlotLayout {
   MatLayout gate, up, down;
-  uint64_t bytes;    // slot row size
+  uint64_t bytes;       // slot row size
 };
 
 static inline uint64_t moe_align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
@@ -42,10 +42,10 @@ static inline MatLayout moe_mat_layout(uint32_t rows, uint32_t k, uint64_t* curs
   m.rows = rows;
   m.k = k;
   m.nb = (k + MOE_BLOCK_K - 1) / MOE_BLOCK_K;
-  m.q_off = *cursor;
-  *cursor = moe_align_up(*cursor + (uint64_t)rows * k / 2, MOE_REGION_ALIGN);
-  m.s_off = *cursor;
-  *cursor = moe_align_up(*cursor + (uint64_t)m.nb * rows * 2, MOE_REGION_ALIGN);
+  m.scale_bytes = m.nb * 32;
+  m.tile_bytes = m.scale_bytes + 8 * k;
+  m.off = *cursor;
+  *cursor = moe_align_up(*cursor + (uint64_t)(rows / 16) * m.tile_bytes, MOE_REGION_ALIGN);
   return m;
 }
 

@@ -8,9 +8,11 @@
 // those experts, not renormalised.
 //
 // Two launch shapes:
-//   small T  : one launch.  CTAs compute split-K partial logits; the last CTA
-//              to arrive (arrival counter, no waiting) finishes softmax/top-k
-//              and the permutation for every token.
+//   small T  : one launch of a thread-block cluster (up to 8 CTAs).  Each CTA
+//              computes the logits of a slice of the experts and writes them
+//              into CTA 0's shared memory (distributed shared memory); after
+//              the cluster barrier CTA 0 finishes softmax/top-k and the
+//              permutation entirely in shared memory.
 //   larger T : logits, top-k (warp per token) and permutation as three launches.
 #include <float.h>
 #include <limits.h>
@@ -21,6 +23,7 @@ namespace {
 
 constexpr int kLogitWarps = 8;    // experts per logits CTA (one warp each)
 constexpr int kMaxEPL = 8;        // experts per lane in top-k: E <= 256
+constexpr int kMaxCluster = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
 DEV_INLINE float dot8(uint4 a, uint4 b) {
@@ -37,32 +40,27 @@ DEV_INLINE float dot8(uint4 a, uint4 b) {
   return s;
 }
 
-DEV_INLINE float sumsq8(uint4 a) { return dot8(a, a); }
+// dot(x_t, w_e) over the whole hidden dimension (one warp).
+DEV_INLINE float warp_dot(const __half* xt, const __half* we, int H, int lane) {
+  float acc = 0.f;
+  for (int kk = lane * 8; kk < H; kk += 256)
+    acc += dot8(__ldg(reinterpret_cast<const uint4*>(xt + kk)), __ldg(reinterpret_cast<const uint4*>(we + kk)));
+  return warp_sum(acc);
+}
 
-// Softmax + top-k of token t (one warp).  Partial logits are read from L2
-// (they may have been written by other CTAs of the same launch).
-DEV_INLINE void topk_token(const FwdCtx& c, int t) {
+// Softmax + top-k of one token (one warp).  lg: the token's E logits (any
+// address space), before bias and pre-norm scale r.  Writes ids/weights to
+// global memory and, when ids_s != NULL, the ids to ids_s too.
+DEV_INLINE void topk_token(const FwdCtx& c, int t, const float* lg, float r, int* ids_s) {
   const int lane = threadIdx.x & 31;
-  const int E = c.E, T = c.T;
-  float r = 1.f;
-  if (c.flags & 2u) {   // PRENORM
-    float ss = 0.f;
-    for (int ks = 0; ks < c.ksplit; ++ks) ss += __ldcg(&c.ss_part[(size_t)ks * T + t]);
-    r = 1.0f / sqrtf(ss / (float)c.H + 1e-6f);
-    if (lane == 0) c.rnorm[t] = r;
-  }
+  const int E = c.E;
   float v[kMaxEPL];
   bool live[kMaxEPL];
 #pragma unroll
   for (int i = 0; i < kMaxEPL; ++i) {
     const int e = lane + 32 * i;
     live[i] = e < E;
-    v[i] = -INFINITY;
-    if (live[i]) {
-      float s = 0.f;
-      for (int ks = 0; ks < c.ksplit; ++ks) s += __ldcg(&c.logit_part[((size_t)ks * T + t) * E + e]);
-      v[i] = s * r + (c.bias ? c.bias[e] : 0.f);
-    }
+    v[i] = live[i] ? lg[e] * r + (c.bias ? c.bias[e] : 0.f) : -INFINITY;
   }
   float m = -INFINITY, selv = -INFINITY;
   int sele = 0;
@@ -92,12 +90,16 @@ DEV_INLINE void topk_token(const FwdCtx& c, int t) {
   if (lane < c.k) {
     c.ids[(size_t)t * c.k + lane] = sele;
     c.topw[(size_t)t * c.k + lane] = (m == -INFINITY) ? 0.f : expf(selv - m) / den;
+    if (ids_s) ids_s[t * c.k + lane] = sele;
   }
 }
 
+DEV_INLINE float prenorm_scale(float ss, int H) { return 1.0f / sqrtf(ss / (float)H + 1e-6f); }
+
 // Stable permutation of the T*k pairs by expert (block-wide; any blockDim that
-// is a multiple of 32).  smem: nwarps*E + 2E + 1 ints.
-DEV_INLINE void permute_block(const FwdCtx& c, int* smem) {
+// is a multiple of 32).  ids: the flat [T*k] expert ids (global or shared).
+// smem: nwarps*E + 2E + 1 ints.
+DEV_INLINE void permute_block(const FwdCtx& c, const int* ids, int* smem) {
   const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = c.E, P = c.T * c.k;
   int* hist = smem;            // [nw][E] counts, then running positions
@@ -107,7 +109,7 @@ DEV_INLINE void permute_block(const FwdCtx& c, int* smem) {
   __syncthreads();
   const int chunk = (P + nw - 1) / nw;
   const int p_beg = min(P, w * chunk), p_end = min(P, p_beg + chunk);
-  for (int p = p_beg + lane; p < p_end; p += 32) atomicAdd(&hist[w * E + c.ids[p]], 1);
+  for (int p = p_beg + lane; p < p_end; p += 32) atomicAdd(&hist[w * E + ids[p]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
@@ -152,7 +154,7 @@ DEV_INLINE void permute_block(const FwdCtx& c, int* smem) {
   for (int base = p_beg; base < p_end; base += 32) {
     const int p = base + lane;
     const bool valid = p < p_end;
-    const int e = valid ? c.ids[p] : -1 - lane;
+    const int e = valid ? ids[p] : -1 - lane;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (valid) {
@@ -203,79 +205,177 @@ DEV_INLINE void permute_block(const FwdCtx& c, int* smem) {
   }
 }
 
-// Partial logits of experts [8*bx, 8*bx+8) over K slice by, tokens of bz.
-__global__ void __launch_bounds__(256) route_logits_kernel(FwdCtx c, int tokens_per_cta, int fused) {
-  extern __shared__ int route_smem[];
+// ------------------------------------------------------------ small T path
+constexpr int kRouteTC = 8;       // tokens per staged x chunk
+
+// Bytes of dynamic smem of route_cluster_kernel.
+size_t route_cluster_smem(int T, int E, int H, int k) {
+  return (size_t)2 * kRouteTC * H * 2 + (size_t)T * E * 4 + (size_t)T * 4 + (size_t)T * k * 4 +
+         (size_t)(8 * E + 2 * E + 1) * 4;
+}
+
+// smem: xbuf [2][kRouteTC][H] f16 | logits [T][E] f32 (CTA 0) | ss [T] f32 (CTA 0)
+//       | ids [T*k] i32 | permutation scratch
+__global__ void __launch_bounds__(256) route_cluster_kernel(FwdCtx c) {
+  extern __shared__ __align__(128) uint8_t rsm[];
+  __shared__ __align__(8) uint64_t xbar[2];
+  __shared__ int s_ok;
+  pdl_wait();      // x may be the output of the preceding grid
+  pdl_trigger();
+  const int T = c.T, E = c.E, H = c.H;
+  __half* xbuf = reinterpret_cast<__half*>(rsm);
+  float* logits = reinterpret_cast<float*>(rsm + (size_t)2 * kRouteTC * H * 2);
+  float* ss = logits + T * E;
+  int* ids_s = reinterpret_cast<int*>(ss + T);
+  int* scratch = ids_s + T * c.k;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int nch = (T + kRouteTC - 1) / kRouteTC;
+  auto issue = [&](int ch) {
+    const int ntok = min(kRouteTC, T - ch * kRouteTC);
+    const uint32_t bytes = (uint32_t)ntok * H * 2;
+    mbar_expect_tx(&xbar[ch & 1], bytes);
+    bulk_g2s(xbuf + (size_t)(ch & 1) * kRouteTC * H, c.x + (size_t)ch * kRouteTC * H, bytes, &xbar[ch & 1]);
+  };
+  if (tid == 0) {
+    s_ok = 1;
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    fence_mbar_init();
+    issue(0);
+    if (nch > 1) issue(1);
+  }
+  cluster_sync();  // every CTA of the cluster is running; barrier init visible
+  const uint32_t rank = cluster_rank(), C = gridDim.x;
+  const int epc = (E + (int)C - 1) / (int)C;
+  for (int ch = 0; ch < nch; ++ch) {
+    const int b = ch & 1;
+    if (!mbar_wait_bounded(&xbar[b], (ch >> 1) & 1, c.status)) s_ok = 0;
+    __syncthreads();
+    const int ntok = min(kRouteTC, T - ch * kRouteTC);
+    const __half* xs = xbuf + (size_t)b * kRouteTC * H;
+    if (s_ok) {
+      for (int ei = w; ei < epc; ei += kLogitWarps) {
+        const int e = (int)rank * epc + ei;
+        if (e >= E) break;
+        const __half* we = c.router_w + (size_t)e * H;
+        float acc[kRouteTC];
+#pragma unroll
+        for (int t = 0; t < kRouteTC; ++t) acc[t] = 0.f;
+        for (int kb = 0; kb < H; kb += 2048) {
+          uint4 wr[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int kk = kb + i * 256 + lane * 8;
+            wr[i] = kk < H ? __ldg(reinterpret_cast<const uint4*>(we + kk)) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int t = 0; t < kRouteTC; ++t) {
+            if (t < ntok) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int kk = kb + i * 256 + lane * 8;
+                if (kk < H) acc[t] += dot8(*reinterpret_cast<const uint4*>(xs + (size_t)t * H + kk), wr[i]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouteTC; ++t) {
+          if (t < ntok) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) st_cluster_f32(map_to_rank(&logits[(ch * kRouteTC + t) * E + e], 0), v);
+          }
+        }
+      }
+      if ((c.flags & 2u) && (int)rank == ch % (int)C && w < ntok) {   // PRENORM sums of squares
+        const __half* xt = xs + (size_t)w * H;
+        float s2 = 0.f;
+        for (int kk = lane * 8; kk < H; kk += 256) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xt + kk);
+          s2 += dot8(v, v);
+        }
+        s2 = warp_sum(s2);
+        if (lane == 0) st_cluster_f32(map_to_rank(&ss[ch * kRouteTC + w], 0), s2);
+      }
+    }
+    __syncthreads();   // every warp is done with xbuf[b]
+    if (tid == 0 && ch + 2 < nch) issue(ch + 2);
+  }
+  cluster_sync();
+  if (rank != 0) return;
+  for (int t = w; t < T; t += blockDim.x >> 5) {
+    float r = 1.f;
+    if (c.flags & 2u) {
+      r = prenorm_scale(ss[t], H);
+      if (lane == 0) c.rnorm[t] = r;
+    }
+    topk_token(c, t, logits + t * E, r, ids_s);
+  }
+  __syncthreads();
+  permute_block(c, ids_s, scratch);
+}
+
+// ------------------------------------------------------------ larger T path
+// Logits of experts [8*bx, 8*bx+8) for tokens of bz (one warp per expert).
+__global__ void __launch_bounds__(256) route_logits_kernel(FwdCtx c, int tokens_per_cta) {
+  pdl_wait();
+  pdl_trigger();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kLogitWarps + w;
   const int H = c.H, T = c.T;
-  const int KC = H / c.ksplit;
-  const int kbeg = blockIdx.y * KC, kend = kbeg + KC;
   const int t0 = blockIdx.z * tokens_per_cta, t1 = min(T, t0 + tokens_per_cta);
   if (e < c.E) {
-    const __half* wr = c.router_w + (size_t)e * H;
+    const __half* we = c.router_w + (size_t)e * H;
     for (int t = t0; t < t1; ++t) {
-      const __half* xt = c.x + (size_t)t * H;
-      float acc = 0.f;
-      for (int kk = kbeg + lane * 8; kk < kend; kk += 256)
-        acc += dot8(__ldg(reinterpret_cast<const uint4*>(xt + kk)), __ldg(reinterpret_cast<const uint4*>(wr + kk)));
-      acc = warp_sum(acc);
-      if (lane == 0) c.logit_part[((size_t)blockIdx.y * T + t) * c.E + e] = acc;
+      const float acc = warp_dot(c.x + (size_t)t * H, we, H, lane);
+      if (lane == 0) c.logit_part[(size_t)t * c.E + e] = acc;
     }
   }
-  if ((c.flags & 2u) && blockIdx.x == 0) {   // PRENORM: partial sums of squares
+  if ((c.flags & 2u) && blockIdx.x == 0) {   // PRENORM: sums of squares
     for (int t = t0 + w; t < t1; t += kLogitWarps) {
       const __half* xt = c.x + (size_t)t * H;
-      float ss = 0.f;
-      for (int kk = kbeg + lane * 8; kk < kend; kk += 256) ss += sumsq8(__ldg(reinterpret_cast<const uint4*>(xt + kk)));
-      ss = warp_sum(ss);
-      if (lane == 0) c.ss_part[(size_t)blockIdx.y * T + t] = ss;
+      const float s2 = warp_dot(xt, xt, H, lane);
+      if (lane == 0) c.ss_part[t] = s2;
     }
   }
-  if (!fused) return;
-  // Last CTA to arrive finishes the routing for every token.
-  __threadfence();
-  __syncthreads();
-  __shared__ unsigned s_last;
-  if (threadIdx.x == 0) {
-    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
-    const unsigned old = atomicAdd(c.route_counter, 1u);
-    s_last = (old == total - 1) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int t = w; t < T; t += blockDim.x >> 5) topk_token(c, t);
-  __syncthreads();
-  permute_block(c, route_smem);
-  if (threadIdx.x == 0) *c.route_counter = 0u;
 }
 
 __global__ void __launch_bounds__(256) route_topk_kernel(FwdCtx c) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t < c.T) topk_token(c, t);
+  if (t >= c.T) return;
+  float r = 1.f;
+  if (c.flags & 2u) {
+    r = prenorm_scale(c.ss_part[t], c.H);
+    if ((threadIdx.x & 31) == 0) c.rnorm[t] = r;
+  }
+  topk_token(c, t, c.logit_part + (size_t)t * c.E, r, nullptr);
 }
 
 __global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c) {
   extern __shared__ int perm_smem[];
-  permute_block(c, perm_smem);
+  pdl_wait();
+  pdl_trigger();
+  permute_block(c, c.ids, perm_smem);
 }
 
 }  // namespace
 
-cudaError_t launch_route(const FwdCtx& c, bool fused, cudaStream_t st) {
-  const dim3 block(256);
-  if (fused) {
-    const dim3 grid((c.E + kLogitWarps - 1) / kLogitWarps, c.ksplit, 1);
-    const size_t smem = (size_t)(8 * c.E + 2 * c.E + 1) * sizeof(int);
-    route_logits_kernel<<<grid, block, smem, st>>>(c, c.T, 1);
-    return cudaGetLastError();
+cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
+  const size_t smem_small = route_cluster_smem(c.T, c.E, c.H, c.k);
+  if (small && smem_small <= 200 * 1024) {
+    int C = (c.E + kLogitWarps - 1) / kLogitWarps;
+    if (C > kMaxCluster) C = kMaxCluster;
+    cudaError_t e = opt_in_smem((const void*)route_cluster_kernel, smem_small);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(route_cluster_kernel, dim3(C), dim3(256), smem_small, st, C, c);
   }
   const int tpc = 16;
-  const dim3 grid((c.E + kLogitWarps - 1) / kLogitWarps, c.ksplit, (c.T + tpc - 1) / tpc);
-  route_logits_kernel<<<grid, block, 0, st>>>(c, tpc, 0);
-  route_topk_kernel<<<(c.T + 7) / 8, block, 0, st>>>(c);
+  const dim3 grid((c.E + kLogitWarps - 1) / kLogitWarps, 1, (c.T + tpc - 1) / tpc);
+  cudaError_t e = launch_pdl(route_logits_kernel, grid, dim3(256), 0, st, 1, c, tpc);
+  if (e == cudaSuccess) e = launch_pdl(route_topk_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, c);
   const size_t smem = (size_t)(32 * c.E + 2 * c.E + 1) * sizeof(int);
-  route_permute_kernel<<<1, 1024, smem, st>>>(c);
-  return cudaGetLastError();
+  if (e == cudaSuccess) e = launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, st, 1, c);
+  return e;
 }

@@ -22,7 +22,8 @@ RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM = 1, 2, 4, 8
 
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
             "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
-            "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens"]
+            "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens",
+            "moe_w4a16_set_stage_events"]
 
 
 class Config(ctypes.Structure):
@@ -63,6 +64,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_get_gemv_max_tokens.argtypes = [vp]
     lib.moe_w4a16_get_gemv_max_tokens.restype = i32
     lib.moe_w4a16_set_gemv_max_tokens.argtypes = [vp, i32]
+    lib.moe_w4a16_set_stage_events.argtypes = [vp, vp]
     _lib = lib
     return lib
 
@@ -173,6 +175,14 @@ class MoELayer:
         self._check(self.lib.moe_w4a16_forward_host(self.h, _ptr(x_host), T, _ptr(router_w), _ptr(bias), flags,
                                                     _ptr(out_host), _stream(stream)))
         return out_host
+
+    def set_stage_events(self, events):
+        """events: 5 torch.cuda.Event(enable_timing=True) (or None to stop)."""
+        if events is None:
+            self._check(self.lib.moe_w4a16_set_stage_events(self.h, None))
+            return
+        arr = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
+        self._check(self.lib.moe_w4a16_set_stage_events(self.h, arr))
 
     def get_status(self):
         """(status code, miss count); synchronises the device and clears the word."""
