@@ -168,6 +168,42 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t
  * the message of the last failed create. */
 MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
 
+/* Limits of moe_w4a16_route_noalloc (its scratch is a fixed 2 MiB device array). */
+#define MOE_W4A16_NOALLOC_MAX_TOKENS 4096
+#define MOE_W4A16_NOALLOC_MAX_LOGITS 262144   /* T * num_experts */
+#define MOE_W4A16_NOALLOC_MAX_PAIRS 65536     /* T * top_k */
+
+/* Routing of one layer (router logits, softmax / top-k, stable permutation:
+ * the same kernels and results as the routing part of moe_w4a16_forward for
+ * T > 64) that allocates nothing and needs no handle.  The Horizon RunMap
+ * pages have no counterpart to this entry point; it exists for callers that
+ * cannot call cudaMalloc: code that runs inside a runtime whose allocator
+ * already owns all device memory (plugins of serving engines that hand out
+ * only pre-planned buffers), code that must not risk the implicit device
+ * synchronisation or the failure of an allocation on a latency-critical
+ * path, and code running while allocation is forbidden.  Creating a handle
+ * allocates, so those callers cannot use moe_w4a16_forward's routing.
+ *   x [T][H] FP16 and router_w [E][H] FP16: device, 16-byte aligned;
+ *   bias [E] FP32 device or NULL; flags: 0 or MOE_W4A16_PRENORM;
+ *   topk_ids [T][k] int32, topk_w [T][k] FP32: device outputs (required);
+ *   sorted_pairs [T*k] int32, expert_offsets [E+1] int32: device outputs or NULL.
+ * Work is enqueued on `stream` (the calling thread's current device).
+ * Scratch lives in one file-scope device array of 2 MiB that every device
+ * which loads the library keeps until the process exits.  The first call on
+ * a device looks up that array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture on the device.
+ * Limits: T <= MOE_W4A16_NOALLOC_MAX_TOKENS, T*E <= ..._MAX_LOGITS,
+ * T*k <= ..._MAX_PAIRS, E <= 256, k <= min(E, 32), H a multiple of 64;
+ * anything beyond returns ERR_INVALID_ARG with a message in
+ * moe_w4a16_last_error(NULL), and nothing is enqueued.  All calls, on any
+ * stream, share the one array: calls whose work overlaps on the GPU race and
+ * give wrong results; serialise them (one stream, or events). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_route_noalloc(const void* x, int32_t T, int32_t hidden,
+                                                       int32_t num_experts, int32_t top_k, const void* router_w,
+                                                       const float* bias, uint32_t flags, int32_t* topk_ids,
+                                                       float* topk_w, int32_t* sorted_pairs,
+                                                       int32_t* expert_offsets, moe_w4a16_stream_t stream);
+
 /* Profiling aid.  With events != NULL (an array of 5 cudaEvent_t created by
  * the caller with timing enabled), every later forward on this handle records
  * them on its stream at the stage boundaries: [0] before routing, [1] after

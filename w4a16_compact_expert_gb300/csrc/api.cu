@@ -112,6 +112,8 @@ int fused_ksplit(int H) {
 
 }  // namespace
 
+void set_handle_free_error(const char* msg) { g_create_err = msg; }
+
 cudaError_t opt_in_smem(const void* func, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
   struct Entry {

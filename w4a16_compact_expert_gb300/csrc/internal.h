@@ -76,6 +76,9 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, cudaStream_t st, const StageEve
 size_t gemv_smem_gateup(int H, int I, int rows);
 size_t gemv_smem_down(int H, int I, int rows);
 
+// Sets the message returned by moe_w4a16_last_error(NULL) (calls without a handle).
+void set_handle_free_error(const char* msg);
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` (once per
 // device and value; thread-safe).
 cudaError_t opt_in_smem(const void* func, size_t bytes);
