@@ -168,9 +168,10 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t
  * the message of the last failed create. */
 MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
 
-/* Limits of moe_w4a16_route_noalloc (its scratch is a fixed 2 MiB device array). */
+/* Limits of moe_w4a16_route_noalloc (its scratch is a fixed 4 MiB device array). */
 #define MOE_W4A16_NOALLOC_MAX_TOKENS 4096
-#define MOE_W4A16_NOALLOC_MAX_LOGITS 262144   /* T * num_experts */
+#define MOE_W4A16_NOALLOC_MAX_HIDDEN 4096
+#define MOE_W4A16_NOALLOC_MAX_LOGITS 786432   /* T * num_experts * ceil(hidden / 256) */
 #define MOE_W4A16_NOALLOC_MAX_PAIRS 65536     /* T * top_k */
 
 /* Routing of one layer (router logits, softmax / top-k, stable permutation:
@@ -188,12 +189,13 @@ MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
  *   topk_ids [T][k] int32, topk_w [T][k] FP32: device outputs (required);
  *   sorted_pairs [T*k] int32, expert_offsets [E+1] int32: device outputs or NULL.
  * Work is enqueued on `stream` (the calling thread's current device).
- * Scratch lives in one file-scope device array of 2 MiB that every device
+ * Scratch lives in one file-scope device array of 4 MiB that every device
  * which loads the library keeps until the process exits.  The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture on the device.
- * Limits: T <= MOE_W4A16_NOALLOC_MAX_TOKENS, T*E <= ..._MAX_LOGITS,
- * T*k <= ..._MAX_PAIRS, E <= 256, k <= min(E, 32), H a multiple of 64;
+ * Limits: T <= MOE_W4A16_NOALLOC_MAX_TOKENS, T*E*ceil(H/256) <=
+ * ..._MAX_LOGITS, T*k <= ..._MAX_PAIRS, E <= 256, k <= min(E, 32), H a
+ * multiple of 64 and <= ..._MAX_HIDDEN;
  * anything beyond returns ERR_INVALID_ARG with a message in
  * moe_w4a16_last_error(NULL), and nothing is enqueued.  All calls, on any
  * stream, share the one array: calls whose work overlaps on the GPU race and

@@ -26,7 +26,7 @@ def qwen():
 
 
 @pytest.mark.parametrize("T", [4, 1, 3, 13, 37, 64, 100, 257])
-@pytest.mark.parametrize("force", [0, F.FORCE_GEMV])
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMV, F.FORCE_GEMM])
 def test_tiny(tiny, T, force):
     x = synth.draw_x(synth.SEED_TINY, T, tiny.shape.hidden)
     err, nflag = gp.check_full(tiny, x, flags=force, max_tokens=max(T, 8))
@@ -34,27 +34,38 @@ def test_tiny(tiny, T, force):
 
 
 @pytest.mark.parametrize("flags", [F.RESIDUAL, F.PRENORM, F.RESIDUAL | F.PRENORM])
-def test_tiny_flags(tiny, flags):
+@pytest.mark.parametrize("force", [F.FORCE_GEMV, F.FORCE_GEMM])
+def test_tiny_flags(tiny, flags, force):
     x = synth.draw_x(synth.SEED_TINY, 20, tiny.shape.hidden)
-    gp.check_full(tiny, x, flags=flags, max_tokens=32)
+    gp.check_full(tiny, x, flags=flags | force, max_tokens=32)
+
+
+def test_tiny_gemm_large_groups():
+    """Experts with more than 256 tokens (several token chunks per expert)."""
+    shape = synth.LayerShape(hidden=256, inter=128, num_experts=4, top_k=2)
+    layer = synth.make_layer(shape, 77)
+    x = synth.draw_x(77, 700, 256)
+    gp.check_full(layer, x, flags=F.FORCE_GEMM, max_tokens=700)
 
 
 @pytest.mark.parametrize("T", [1, 4, 16])
-def test_olmoe_decode(olmoe, T):
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMM])
+def test_olmoe_decode(olmoe, T, force):
     x = synth.draw_x(synth.SEED_OLMOE_DECODE, T, olmoe.shape.hidden)
-    err, nflag = gp.check_full(olmoe, x, max_tokens=2048)
+    err, nflag = gp.check_full(olmoe, x, flags=force, max_tokens=2048)
     print(f"olmoe T={T} rel={err:.2e} flagged={nflag}")
 
 
 @pytest.mark.parametrize("T", [1, 8, 32])
-def test_qwen_partial(qwen, T):
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMM])
+def test_qwen_partial(qwen, T, force):
     x = synth.draw_x(synth.SEED_QWEN_PARTIAL, T, qwen.shape.hidden)
-    err, nflag = gp.check_full(qwen, x, max_tokens=64)
+    err, nflag = gp.check_full(qwen, x, flags=force, max_tokens=64)
     print(f"qwen T={T} rel={err:.2e} flagged={nflag}")
 
 
 @pytest.mark.parametrize("variant", [1, 2])
-@pytest.mark.parametrize("force", [F.FORCE_GEMV])
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMV])
 def test_olmoe_prefill_sampled(variant, force):
     layer = synth.olmoe_prefill_layer(variant)
     seed = synth.SEED_OLMOE_PREFILL if variant == 1 else synth.SEED_OLMOE_PREFILL_SKEW

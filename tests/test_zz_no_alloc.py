@@ -83,3 +83,6 @@ def test_route_noalloc_rejects_sizes_beyond_the_limit(lib):
     st = lib.moe_w4a16_route_noalloc(x.data_ptr(), 4096, 256, 256, 8, rw.data_ptr(), None, 0, ids.data_ptr(),
                                      w.data_ptr(), None, None, s)
     assert st == moe_w4a16.ERR_INVALID_ARG and b"MAX_LOGITS" in lib.moe_w4a16_last_error(None)
+    st = lib.moe_w4a16_route_noalloc(x.data_ptr(), 8, 8192, 64, 8, rw.data_ptr(), None, 0, ids.data_ptr(),
+                                     w.data_ptr(), None, None, s)
+    assert st == moe_w4a16.ERR_INVALID_ARG and b"MAX_HIDDEN" in lib.moe_w4a16_last_error(None)

@@ -38,6 +38,7 @@ struct moe_w4a16_handle {
   int32_t* sorted = nullptr;
   int32_t* p2r = nullptr;
   int32_t* act = nullptr;            // 5 arrays of E (+1) ints, see fill_ctx
+  __half* xp = nullptr;
   __half* hbuf = nullptr;
   float* ybuf = nullptr;
   unsigned* counters = nullptr;      // [1 + H/32]
@@ -47,6 +48,7 @@ struct moe_w4a16_handle {
   __half* x_dev = nullptr;           // forward_host staging
   __half* out_dev = nullptr;
   StageEvents events{};
+  PoolMaps maps{};
   std::vector<void*> allocs;
   std::string err;
 };
@@ -193,7 +195,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   h->lay = moe_slot_layout(c.hidden, c.inter);
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device);
   h->ksplit_fused = fused_ksplit(c.hidden);
-  h->gemv_max_tokens = c.max_tokens;
+  h->gemv_max_tokens = 64;
   h->packed.assign(c.num_slots, 0);
   h->h_table.assign(c.num_experts, -1);
   const size_t H = c.hidden, I = c.inter, E = c.num_experts, T = c.max_tokens, P = T * c.top_k;
@@ -204,8 +206,9 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   if (e == cudaSuccess) e = dalloc(h, &(ptr), (n))
   ALLOC(h->pool, (size_t)c.num_slots * h->lay.bytes);
   ALLOC(h->d_table, E);
-  ALLOC(h->logit_part, 8 * T * E);
-  ALLOC(h->ss_part, 8 * T);
+  const size_t kslices = std::max<size_t>(8, (H + 255) / 256);   // router K slices
+  ALLOC(h->logit_part, kslices * T * E);
+  ALLOC(h->ss_part, kslices * T);
   ALLOC(h->rnorm, T);
   ALLOC(h->ids, P);
   ALLOC(h->topw, P);
@@ -213,6 +216,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   ALLOC(h->sorted, P);
   ALLOC(h->p2r, P);
   ALLOC(h->act, 5 * E + 2 + 1);
+  ALLOC(h->xp, P * H);
   ALLOC(h->hbuf, P * I);
   ALLOC(h->ybuf, P * H);
   ALLOC(h->counters, 1 + H / 32);
@@ -225,6 +229,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(h->d_table, 0xff, E * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) h->maps = make_pool_maps(h->pool, h->lay, c.num_slots);
   if (e != cudaSuccess) {
     const bool oom = e == cudaErrorMemoryAllocation;
     cudaGetLastError();
@@ -366,6 +371,7 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.act_count = h->act + 3 * E;
   c.act_tile = h->act + 4 * E;        // E + 1 entries
   c.n_active = h->act + 5 * E + 1;
+  c.xp = h->xp;
   c.hbuf = h->hbuf;
   c.ybuf = h->ybuf;
   c.route_counter = h->counters;
@@ -402,10 +408,12 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.bias = bias;
   c.flags = flags;
   c.out = static_cast<__half*>(out);
-  const bool gemm = (flags & MOE_W4A16_FORCE_GEMM) || (!(flags & MOE_W4A16_FORCE_GEMV) && T > h->gemv_max_tokens);
+  const bool gemm = (flags & MOE_W4A16_FORCE_GEMM) ||
+                    (!(flags & MOE_W4A16_FORCE_GEMV) && T > h->gemv_max_tokens &&
+                     gemm_shapes_supported(h->cfg.hidden, h->cfg.inter));
   const bool fused_route = T <= ROUTE_FUSED_MAX_T;
   c.ksplit = 1;
-  c.tile_tokens = 128;
+  c.tile_tokens = 256;   // token chunk of the grouped GEMM
   int ma = c.E;
   if ((long long)T * c.k < ma) ma = T * c.k;
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
@@ -414,7 +422,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (e == cudaSuccess) e = launch_route(c, fused_route, st);
   if (e == cudaSuccess) e = record_stage(h->events, 1, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
-  e = gemm ? launch_gemm_experts(c, st, h->events) : launch_gemv_experts(c, st, h->events);
+  e = gemm ? launch_gemm_experts(c, h->maps, st, h->events) : launch_gemv_experts(c, st, h->events);
   if (e == cudaErrorNotSupported) return fail(h, MOE_W4A16_ERR_UNSUPPORTED, "grouped GEMM path not available");
   if (e != cudaSuccess) return cuda_fail(h, e, "expert launch");
   const size_t P = (size_t)T * c.k;

@@ -1,5 +1,6 @@
 // Internal (non-ABI) declarations shared by the host runtime and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -40,6 +41,7 @@ struct FwdCtx {
   int32_t* n_active;           // [1]
   int tile_tokens;             // token tile of the grouped GEMM
   // expert workspaces
+  __half* xp;                  // [T*k][H] activations gathered in sorted-row order (prefill)
   __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
   unsigned* route_counter;     // [1] arrival counter (self-resetting)
@@ -66,8 +68,18 @@ cudaError_t record_stage(const StageEvents& se, int i, cudaStream_t st);
 // gemv.cu: decode regime (gate/up kernel, then down kernel with the combine)
 cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
 
-// gemm_tc.cu: prefill regime (gate/up GEMM, down GEMM, combine)
-cudaError_t launch_gemm_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
+// gemm_tc.cu: prefill regime (gather, gate/up GEMM, down GEMM, combine)
+bool gemm_shapes_supported(int H, int I);
+
+// TMA descriptors of the compact int4 chunks of gate, up and down over the
+// whole slot pool (4-D: 512-byte chunk, K chunk, row tile, slot).  Built once
+// per handle.
+struct PoolMaps {
+  CUtensorMap q[3];
+  bool ok;
+};
+PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slots);
+cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_t st, const StageEvents& se);
 
 // route: the largest T handled by the single-launch cluster router
 #define ROUTE_FUSED_MAX_T 64

@@ -13,21 +13,22 @@
 #include "../../include/moe_w4a16.h"
 #include "internal.h"
 
-#define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kMaxTokens = MOE_W4A16_NOALLOC_MAX_TOKENS;
-constexpr long long kMaxLogits = MOE_W4A16_NOALLOC_MAX_LOGITS;   // T * E
+constexpr long long kMaxLogits = MOE_W4A16_NOALLOC_MAX_LOGITS;   // T * E * ceil(H / 256)
+constexpr int kMaxHidden = MOE_W4A16_NOALLOC_MAX_HIDDEN;
 constexpr int kMaxPairs = MOE_W4A16_NOALLOC_MAX_PAIRS;           // T * k
 constexpr int kMaxE = 256;
 
 // Byte offsets inside g_route_scratch.
-constexpr size_t kOffLogits = 0;                                    // [T][E] f32
-constexpr size_t kOffSs = kOffLogits + (size_t)kMaxLogits * 4;      // [T] f32
-constexpr size_t kOffRnorm = kOffSs + (size_t)kMaxTokens * 4;       // [T] f32
+constexpr size_t kOffLogits = 0;                                    // [H/256][T][E] f32 partial logits
+constexpr size_t kOffSs = kOffLogits + (size_t)kMaxLogits * 4;      // [H/256][T] f32
+constexpr size_t kOffRnorm = kOffSs + (size_t)kMaxTokens * (kMaxHidden / 256) * 4;   // [T] f32
 constexpr size_t kOffSorted = kOffRnorm + (size_t)kMaxTokens * 4;   // [T*k] i32 (when the caller passes none)
 constexpr size_t kOffP2r = kOffSorted + (size_t)kMaxPairs * 4;      // [T*k] i32
 constexpr size_t kOffOffsets = kOffP2r + (size_t)kMaxPairs * 4;     // [E+1] i32 (when the caller passes none)
@@ -65,11 +66,13 @@ extern "C" MOE_W4A16_API moe_w4a16_status moe_w4a16_route_noalloc(
     const float* bias, uint32_t flags, int32_t* topk_ids, float* topk_w, int32_t* sorted_pairs,
     int32_t* expert_offsets, moe_w4a16_stream_t stream) {
   if (T < 0 || T > kMaxTokens) return reject("route_noalloc: T outside [0, MOE_W4A16_NOALLOC_MAX_TOKENS]");
-  if (hidden < 64 || hidden % 64) return reject("route_noalloc: hidden must be a positive multiple of 64");
+  if (hidden < 64 || hidden % 64 || hidden > kMaxHidden)
+    return reject("route_noalloc: hidden must be a multiple of 64 in [64, MOE_W4A16_NOALLOC_MAX_HIDDEN]");
   if (num_experts < 1 || num_experts > kMaxE) return reject("route_noalloc: num_experts outside [1, 256]");
   if (top_k < 1 || top_k > 32 || top_k > num_experts) return reject("route_noalloc: top_k outside [1, min(E, 32)]");
-  if ((long long)T * num_experts > kMaxLogits)
-    return reject("route_noalloc: T * num_experts exceeds MOE_W4A16_NOALLOC_MAX_LOGITS");
+  const long long kslices = (hidden + 255) / 256;   // K slices of the router logits
+  if ((long long)T * num_experts * kslices > kMaxLogits)
+    return reject("route_noalloc: T * num_experts * ceil(hidden / 256) exceeds MOE_W4A16_NOALLOC_MAX_LOGITS");
   if ((long long)T * top_k > kMaxPairs) return reject("route_noalloc: T * top_k exceeds MOE_W4A16_NOALLOC_MAX_PAIRS");
   if (flags & ~(uint32_t)MOE_W4A16_PRENORM) return reject("route_noalloc: only the PRENORM flag applies");
   if (T == 0) return MOE_W4A16_OK;

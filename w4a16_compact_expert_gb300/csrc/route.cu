@@ -99,7 +99,8 @@ DEV_INLINE float prenorm_scale(float ss, int H) { return 1.0f / sqrtf(ss / (floa
 // Stable permutation of the T*k pairs by expert (block-wide; any blockDim that
 // is a multiple of 32).  ids: the flat [T*k] expert ids (global or shared).
 // smem: nwarps*E + 2E + 1 ints.
-DEV_INLINE void permute_block(const FwdCtx& c, const int* ids, int* smem) {
+template <typename IdT>
+DEV_INLINE void permute_block(const FwdCtx& c, const IdT* ids, int* smem) {
   const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = c.E, P = c.T * c.k;
   int* hist = smem;            // [nw][E] counts, then running positions
@@ -109,7 +110,7 @@ DEV_INLINE void permute_block(const FwdCtx& c, const int* ids, int* smem) {
   __syncthreads();
   const int chunk = (P + nw - 1) / nw;
   const int p_beg = min(P, w * chunk), p_end = min(P, p_beg + chunk);
-  for (int p = p_beg + lane; p < p_end; p += 32) atomicAdd(&hist[w * E + ids[p]], 1);
+  for (int p = p_beg + lane; p < p_end; p += 32) atomicAdd(&hist[w * E + (int)ids[p]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
@@ -154,7 +155,7 @@ DEV_INLINE void permute_block(const FwdCtx& c, const int* ids, int* smem) {
   for (int base = p_beg; base < p_end; base += 32) {
     const int p = base + lane;
     const bool valid = p < p_end;
-    const int e = valid ? ids[p] : -1 - lane;
+    const int e = valid ? (int)ids[p] : -1 - lane;
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (valid) {
@@ -316,48 +317,114 @@ __global__ void __launch_bounds__(256) route_cluster_kernel(FwdCtx c) {
 }
 
 // ------------------------------------------------------------ larger T path
-// Logits of experts [8*bx, 8*bx+8) for tokens of bz (one warp per expert).
-__global__ void __launch_bounds__(256) route_logits_kernel(FwdCtx c, int tokens_per_cta) {
+constexpr int kRouteKC = 256;     // K slice of one logits CTA
+constexpr int kRouteTile = 64;    // tokens x experts of one logits CTA
+
+// Partial logits of a 64-token x 64-expert tile over one 256-wide K slice on
+// the tensor cores (16x8x16 MMA, FP16 in, FP32 accumulate); the slices are
+// summed in fixed order by the top-k kernel.
+__global__ void __launch_bounds__(128) route_logits_mma_kernel(FwdCtx c) {
+  extern __shared__ __align__(16) uint8_t lsm[];
+  pdl_wait();
+  pdl_trigger();
+  constexpr int S = kRouteKC + 8;   // padded row stride (halves): conflict-free fragment reads
+  __half* xs = reinterpret_cast<__half*>(lsm);
+  __half* ws = xs + kRouteTile * S;
+  const int T = c.T, E = c.E, H = c.H;
+  const int t0 = blockIdx.x * kRouteTile, e0 = blockIdx.y * kRouteTile, ks = blockIdx.z;
+  const int k0 = ks * kRouteKC, kc = min(kRouteKC, H - k0);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, cq = lane & 3;
+  const int vpr = kc / 8;   // 16-byte vectors per row
+  for (int i = tid; i < kRouteTile * vpr; i += blockDim.x) {
+    const int r = i / vpr, v = i % vpr;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const int t = t0 + r, e = e0 + r;
+    *reinterpret_cast<uint4*>(xs + r * S + v * 8) =
+        t < T ? __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)t * H + k0) + v) : z;
+    *reinterpret_cast<uint4*>(ws + r * S + v * 8) =
+        e < E ? __ldg(reinterpret_cast<const uint4*>(c.router_w + (size_t)e * H + k0) + v) : z;
+  }
+  __syncthreads();
+  float acc[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+  const __half* xa = xs + (w * 16 + g) * S + 2 * cq;
+  for (int kk = 0; kk < kc; kk += 16) {
+    uint32_t a[4];
+    a[0] = *reinterpret_cast<const uint32_t*>(xa + kk);
+    a[1] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk);
+    a[2] = *reinterpret_cast<const uint32_t*>(xa + kk + 8);
+    a[3] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk + 8);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const __half* wb = ws + (nt * 8 + g) * S + kk + 2 * cq;
+      mma_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(wb), *reinterpret_cast<const uint32_t*>(wb + 8));
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + w * 16 + g + (i >= 2 ? 8 : 0), e = e0 + nt * 8 + 2 * cq + (i & 1);
+      if (t < T && e < E) c.logit_part[((size_t)ks * T + t) * E + e] = acc[nt][i];
+    }
+  }
+  if ((c.flags & 2u) && blockIdx.y == 0) {   // PRENORM: partial sums of squares
+    for (int r = w; r < kRouteTile; r += 4) {
+      float s2 = 0.f;
+      for (int kk = lane * 2; kk < kc; kk += 64) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(xs + r * S + kk));
+        s2 = fmaf(f.x, f.x, fmaf(f.y, f.y, s2));
+      }
+      s2 = warp_sum(s2);
+      if (lane == 0 && t0 + r < T) c.ss_part[(size_t)ks * T + t0 + r] = s2;
+    }
+  }
+}
+
+// One warp per token: sums the K slices of its logits (fixed order), then
+// softmax / top-k.
+__global__ void __launch_bounds__(256) route_topk_kernel(FwdCtx c) {
+  __shared__ float lg[8][256];
   pdl_wait();
   pdl_trigger();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kLogitWarps + w;
-  const int H = c.H, T = c.T;
-  const int t0 = blockIdx.z * tokens_per_cta, t1 = min(T, t0 + tokens_per_cta);
-  if (e < c.E) {
-    const __half* we = c.router_w + (size_t)e * H;
-    for (int t = t0; t < t1; ++t) {
-      const float acc = warp_dot(c.x + (size_t)t * H, we, H, lane);
-      if (lane == 0) c.logit_part[(size_t)t * c.E + e] = acc;
-    }
-  }
-  if ((c.flags & 2u) && blockIdx.x == 0) {   // PRENORM: sums of squares
-    for (int t = t0 + w; t < t1; t += kLogitWarps) {
-      const __half* xt = c.x + (size_t)t * H;
-      const float s2 = warp_dot(xt, xt, H, lane);
-      if (lane == 0) c.ss_part[t] = s2;
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256) route_topk_kernel(FwdCtx c) {
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int t = blockIdx.x * 8 + w;
   if (t >= c.T) return;
+  for (int e = lane; e < c.E; e += 32) {
+    float s = 0.f;
+    for (int ks = 0; ks < c.ksplit; ++ks) s += c.logit_part[((size_t)ks * c.T + t) * c.E + e];
+    lg[w][e] = s;
+  }
   float r = 1.f;
   if (c.flags & 2u) {
-    r = prenorm_scale(c.ss_part[t], c.H);
-    if ((threadIdx.x & 31) == 0) c.rnorm[t] = r;
+    float ss = 0.f;
+    for (int ks = 0; ks < c.ksplit; ++ks) ss += c.ss_part[(size_t)ks * c.T + t];
+    r = prenorm_scale(ss, c.H);
+    if (lane == 0) c.rnorm[t] = r;
   }
-  topk_token(c, t, c.logit_part + (size_t)t * c.E, r, nullptr);
+  __syncwarp();
+  topk_token(c, t, lg[w], r, nullptr);
 }
 
-__global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c) {
-  extern __shared__ int perm_smem[];
+// One CTA: the expert ids are staged in shared memory (one byte each), then
+// histogram, scan and stable scatter run out of shared memory.
+__global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c, int ids_in_smem) {
+  extern __shared__ __align__(16) int perm_smem[];
   pdl_wait();
   pdl_trigger();
-  permute_block(c, c.ids, perm_smem);
+  const int P = c.T * c.k;
+  if (ids_in_smem) {
+    uint8_t* ids8 = reinterpret_cast<uint8_t*>(perm_smem);
+    int* scratch = perm_smem + (P + 15) / 16 * 4;
+    for (int p = threadIdx.x; p < P; p += blockDim.x) ids8[p] = (uint8_t)c.ids[p];
+    __syncthreads();
+    permute_block(c, ids8, scratch);
+  } else {
+    permute_block(c, c.ids, perm_smem);
+  }
 }
 
 }  // namespace
@@ -371,11 +438,20 @@ cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     return launch_pdl(route_cluster_kernel, dim3(C), dim3(256), smem_small, st, C, c);
   }
-  const int tpc = 16;
-  const dim3 grid((c.E + kLogitWarps - 1) / kLogitWarps, 1, (c.T + tpc - 1) / tpc);
-  cudaError_t e = launch_pdl(route_logits_kernel, grid, dim3(256), 0, st, 1, c, tpc);
-  if (e == cudaSuccess) e = launch_pdl(route_topk_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, c);
-  const size_t smem = (size_t)(32 * c.E + 2 * c.E + 1) * sizeof(int);
-  if (e == cudaSuccess) e = launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, st, 1, c);
+  FwdCtx cc = c;
+  cc.ksplit = (c.H + kRouteKC - 1) / kRouteKC;
+  const size_t lsmem = (size_t)2 * kRouteTile * (kRouteKC + 8) * sizeof(__half);
+  cudaError_t e = opt_in_smem((const void*)route_logits_mma_kernel, lsmem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((c.T + kRouteTile - 1) / kRouteTile, (c.E + kRouteTile - 1) / kRouteTile, cc.ksplit);
+  e = launch_pdl(route_logits_mma_kernel, grid, dim3(128), lsmem, st, 1, cc);
+  if (e == cudaSuccess) e = launch_pdl(route_topk_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, cc);
+  const int P = c.T * c.k;
+  const size_t scratch = (size_t)(32 * c.E + 2 * c.E + 1) * sizeof(int);
+  const size_t smem_ids = (size_t)(P + 15) / 16 * 16 + scratch;
+  const int in_smem = smem_ids <= 200 * 1024;
+  const size_t smem = in_smem ? smem_ids : scratch;
+  if (e == cudaSuccess) e = opt_in_smem((const void*)route_permute_kernel, smem);
+  if (e == cudaSuccess) e = launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, st, 1, cc, in_smem);
   return e;
 }
