@@ -88,6 +88,8 @@ typedef enum {
 #define MOE_W4A16_PRENORM    2u   /* experts and router see x / rms(x) */
 #define MOE_W4A16_FORCE_GEMV 4u   /* decode kernels whatever T is */
 #define MOE_W4A16_FORCE_GEMM 8u   /* tensor-core grouped GEMM whatever T is */
+#define MOE_W4A16_UNFUSED   16u   /* decode regime as separate route / gate-up / down launches
+                                     instead of the single cooperative launch used for T <= 64 */
 
 typedef struct {
   int32_t hidden;       /* H: multiple of 64, >= 64 */

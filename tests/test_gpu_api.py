@@ -26,11 +26,12 @@ def test_t0_is_noop(tiny):
         m.close()
 
 
-def test_deterministic_and_slot_relabel_invariant(tiny):
+@pytest.mark.parametrize("flags", [0, F.UNFUSED, F.FORCE_GEMM])
+def test_deterministic_and_slot_relabel_invariant(tiny, flags):
     x = synth.draw_x(7, 33, 256)
     m = gp.make_handle(tiny, 64)
-    out1, d1 = gp.gpu_forward(m, tiny, x)
-    out2, d2 = gp.gpu_forward(m, tiny, x)
+    out1, d1 = gp.gpu_forward(m, tiny, x, flags)
+    out2, d2 = gp.gpu_forward(m, tiny, x, flags)
     m.close()
     assert np.array_equal(out1, out2) and np.array_equal(d1["sorted_pairs"], d2["sorted_pairs"])
     # same experts at a permuted set of slot rows (and two spare rows never used)
@@ -44,7 +45,7 @@ def test_deterministic_and_slot_relabel_invariant(tiny):
         m2.pack_experts(4, *(a[:1] for a in ex))
         m2.pack_experts(6, *(a[1:2] for a in ex))
         m2.set_slot_table(perm)
-        out3, _ = gp.gpu_forward(m2, tiny, x)
+        out3, _ = gp.gpu_forward(m2, tiny, x, flags)
     finally:
         m2.close()
     assert np.array_equal(out1, out3)
@@ -60,7 +61,27 @@ def test_zero_input_gives_zero(tiny):
     assert np.all(out == 0)
 
 
-def test_routed_absent_expert_counts_misses(tiny):
+def test_all_routed_experts_absent(tiny):
+    """Only two experts resident and none of them routed: out = x (RESIDUAL) or 0."""
+    x = synth.draw_x(12, 6, 256)
+    m = gp.make_handle(tiny, 8)
+    try:
+        m.set_slot_table([-1, -1, -1, -1, -1, -1, 6, 7])
+        bias = np.zeros(8, np.float32)
+        bias[6:] = -1e4          # never routed
+        for flags in (0, F.RESIDUAL, F.UNFUSED, F.RESIDUAL | F.UNFUSED, F.FORCE_GEMM | F.RESIDUAL):
+            out, _ = m.forward(gp.to_dev(x), gp.to_dev(tiny.router_w), gp.to_dev(bias), flags, debug=True)
+            got = out.float().cpu().numpy()
+            expect = x.astype(np.float32) if flags & F.RESIDUAL else np.zeros_like(got)
+            assert np.array_equal(got, expect), flags
+        st, miss = m.get_status()
+        assert st == F.ERR_NOT_RESIDENT and miss == 5 * 6 * 2
+    finally:
+        m.close()
+
+
+@pytest.mark.parametrize("flags", [0, F.UNFUSED, F.FORCE_GEMM])
+def test_routed_absent_expert_counts_misses(tiny, flags):
     x = synth.draw_x(11, 24, 256)
     table = tiny.expert_to_slot.copy()
     table[3] = -1
@@ -68,7 +89,7 @@ def test_routed_absent_expert_counts_misses(tiny):
     m = gp.make_handle(tiny, 32)
     try:
         m.set_slot_table(table)
-        out, dbg = gp.gpu_forward(m, tiny, x)
+        out, dbg = gp.gpu_forward(m, tiny, x, flags)
         st, miss = m.get_status()
         st2, miss2 = m.get_status()
     finally:

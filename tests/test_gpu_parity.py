@@ -26,7 +26,7 @@ def qwen():
 
 
 @pytest.mark.parametrize("T", [4, 1, 3, 13, 37, 64, 100, 257])
-@pytest.mark.parametrize("force", [0, F.FORCE_GEMV, F.FORCE_GEMM])
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMV | F.UNFUSED, F.FORCE_GEMM])
 def test_tiny(tiny, T, force):
     x = synth.draw_x(synth.SEED_TINY, T, tiny.shape.hidden)
     err, nflag = gp.check_full(tiny, x, flags=force, max_tokens=max(T, 8))
@@ -34,7 +34,7 @@ def test_tiny(tiny, T, force):
 
 
 @pytest.mark.parametrize("flags", [F.RESIDUAL, F.PRENORM, F.RESIDUAL | F.PRENORM])
-@pytest.mark.parametrize("force", [F.FORCE_GEMV, F.FORCE_GEMM])
+@pytest.mark.parametrize("force", [0, F.FORCE_GEMV | F.UNFUSED, F.FORCE_GEMM])
 def test_tiny_flags(tiny, flags, force):
     x = synth.draw_x(synth.SEED_TINY, 20, tiny.shape.hidden)
     gp.check_full(tiny, x, flags=flags | force, max_tokens=32)
@@ -49,7 +49,7 @@ def test_tiny_gemm_large_groups():
 
 
 @pytest.mark.parametrize("T", [1, 4, 16])
-@pytest.mark.parametrize("force", [0, F.FORCE_GEMM])
+@pytest.mark.parametrize("force", [0, F.UNFUSED, F.FORCE_GEMM])
 def test_olmoe_decode(olmoe, T, force):
     x = synth.draw_x(synth.SEED_OLMOE_DECODE, T, olmoe.shape.hidden)
     err, nflag = gp.check_full(olmoe, x, flags=force, max_tokens=2048)
@@ -57,7 +57,7 @@ def test_olmoe_decode(olmoe, T, force):
 
 
 @pytest.mark.parametrize("T", [1, 8, 32])
-@pytest.mark.parametrize("force", [0, F.FORCE_GEMM])
+@pytest.mark.parametrize("force", [0, F.UNFUSED, F.FORCE_GEMM])
 def test_qwen_partial(qwen, T, force):
     x = synth.draw_x(synth.SEED_QWEN_PARTIAL, T, qwen.shape.hidden)
     err, nflag = gp.check_full(qwen, x, flags=force, max_tokens=64)

@@ -14,7 +14,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/moe_w4a16.h"
+#include "moe_w4a16.h"
 #include "internal.h"
 
 struct moe_w4a16_handle {
@@ -22,6 +22,7 @@ struct moe_w4a16_handle {
   SlotLayout lay{};
   int num_sms = 0;
   int ksplit_fused = 1;
+  int max_smem = 0;                  // opt-in shared memory per block
   int32_t gemv_max_tokens = 0;
   uint8_t* pool = nullptr;
   std::vector<uint8_t> packed;      // per slot: 1 once packed
@@ -41,7 +42,7 @@ struct moe_w4a16_handle {
   __half* xp = nullptr;
   __half* hbuf = nullptr;
   float* ybuf = nullptr;
-  unsigned* counters = nullptr;      // [1 + H/32]
+  unsigned* counters = nullptr;      // [1 + H/32] arrival counters, then [20] grid-barrier words
   DevStatus* status = nullptr;
   uint8_t* stage = nullptr;          // pack staging for host sources
   size_t stage_bytes = 0;
@@ -194,6 +195,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   h->cfg = c;
   h->lay = moe_slot_layout(c.hidden, c.inter);
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device);
+  cudaDeviceGetAttribute(&h->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
   h->ksplit_fused = fused_ksplit(c.hidden);
   h->gemv_max_tokens = 64;
   h->packed.assign(c.num_slots, 0);
@@ -219,13 +221,13 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   ALLOC(h->xp, P * H);
   ALLOC(h->hbuf, P * I);
   ALLOC(h->ybuf, P * H);
-  ALLOC(h->counters, 1 + H / 32);
+  ALLOC(h->counters, 1 + H / 32 + 20);
   ALLOC(h->status, 1);
   ALLOC(h->stage, h->stage_bytes);
   ALLOC(h->x_dev, T * H);
   ALLOC(h->out_dev, T * H);
 #undef ALLOC
-  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, (1 + H / 32) * sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, (1 + H / 32 + 20) * sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(h->d_table, 0xff, E * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -376,6 +378,7 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.ybuf = h->ybuf;
   c.route_counter = h->counters;
   c.down_counters = h->counters + 1;
+  c.grid_sync = h->counters + 1 + h->cfg.hidden / 32;
   c.status = h->status;
   c.num_sms = h->num_sms;
 }
@@ -386,7 +389,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (!h) return MOE_W4A16_ERR_INVALID_ARG;
   if (T < 0 || T > h->cfg.max_tokens)
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "T=" + std::to_string(T) + " outside [0, max_tokens]");
-  if (flags & ~15u) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "unknown flag bits");
+  if (flags & ~31u) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "unknown flag bits");
   if ((flags & MOE_W4A16_FORCE_GEMV) && (flags & MOE_W4A16_FORCE_GEMM))
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "FORCE_GEMV and FORCE_GEMM are exclusive");
   if (T == 0) return MOE_W4A16_OK;
@@ -418,11 +421,20 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if ((long long)T * c.k < ma) ma = T * c.k;
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
   c.max_active = ma;
+  const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
   cudaError_t e = record_stage(h->events, 0, st);
-  if (e == cudaSuccess) e = launch_route(c, fused_route, st);
+  if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);
   if (e == cudaSuccess) e = record_stage(h->events, 1, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
-  e = gemm ? launch_gemm_experts(c, h->maps, st, h->events) : launch_gemv_experts(c, st, h->events);
+  if (fused) {
+    e = launch_fused_decode(c, st, h->events);
+    if (e == cudaErrorNotSupported) {   // cannot be co-resident here: separate launches
+      e = launch_route(c, fused_route, st);
+      if (e == cudaSuccess) e = launch_gemv_experts(c, st, h->events);
+    }
+  } else {
+    e = gemm ? launch_gemm_experts(c, h->maps, st, h->events) : launch_gemv_experts(c, st, h->events);
+  }
   if (e == cudaErrorNotSupported) return fail(h, MOE_W4A16_ERR_UNSUPPORTED, "grouped GEMM path not available");
   if (e != cudaSuccess) return cuda_fail(h, e, "expert launch");
   const size_t P = (size_t)T * c.k;
@@ -467,7 +479,11 @@ moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t* miss_count) 
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(h, e, "get_status");
   if (miss_count) *miss_count = (int64_t)s.miss;
-  if (s.flags & STATUS_TIMEOUT) return fail(h, MOE_W4A16_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (s.flags & STATUS_TIMEOUT) {   // barriers and counters may be mid-use: start them afresh
+    cudaMemset(h->counters, 0, (1 + h->cfg.hidden / 32 + 20) * sizeof(unsigned));
+    cudaDeviceSynchronize();
+    return fail(h, MOE_W4A16_ERR_TIMEOUT, "a bounded device wait gave up");
+  }
   if (s.flags & STATUS_MISS) return fail(h, MOE_W4A16_ERR_NOT_RESIDENT, "a routed expert had no slot");
   return MOE_W4A16_OK;
 }

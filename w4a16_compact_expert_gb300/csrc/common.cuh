@@ -59,7 +59,7 @@ DEV_INLINE float warp_sum(float v) {
   return v;
 }
 
-DEV_INLINE float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+DEV_INLINE float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Start of 16-row tile rt of a matrix in a slot row (layout.h).
 DEV_INLINE const uint8_t* tile_ptr(const uint8_t* slot_base, const MatLayout& m, int rt) {

@@ -31,15 +31,18 @@ namespace {
 constexpr int kMTile = 128;     // weight rows per tile (MMA M)
 constexpr int kNMax = 256;      // tokens per tile (MMA N, max)
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of FP16)
-constexpr int kStagesRaw = 4;
-constexpr int kStagesA = 2;
-constexpr int kThreads = 320;   // warps 0-3 dequant, 4-7 epilogue, 8 producer, 9 MMA
+constexpr int kStagesA = 3;
+constexpr int kDqWarps = 8;     // warps 0-7 dequant (one 16-row tile each)
+constexpr int kThreads = 480;   // + warps 8-11 epilogue, 12 int4 producer, 13 token producer, 14 MMA
+constexpr int kWarpEpi = 8, kWarpProd = 12, kWarpProdB = 13, kWarpMma = 14;
+constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;
 
 template <bool GU>
 struct Cfg {
   static constexpr int kMats = GU ? 2 : 1;
-  static constexpr int kStagesB = GU ? 3 : 4;
+  static constexpr int kStagesB = GU ? 2 : 4;
+  static constexpr int kStagesRaw = GU ? 6 : 10;   // int4 chunks come from HBM: deepest ring
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
   static constexpr int kBBytes = kNMax * kBK * 2;         // 32 KB
@@ -47,9 +50,11 @@ struct Cfg {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStagesA * kABytes;
   static constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
-  static constexpr int kOffBar = kOffRaw + kStagesRaw * kRawBytes;
+  static constexpr int kOffSched = kOffRaw + kStagesRaw * kRawBytes;   // 4 x (kMaxE + 1) ints + count
+  static constexpr int kOffBar = kOffSched + (4 * (kMaxE + 1) + 4) * 4;
   static constexpr int kNumBars = 2 * kStagesRaw + 2 * kStagesA + 2 * kStagesB + 4;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;   // + TMEM slot + alignment slack
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
 struct Ring {
@@ -67,26 +72,63 @@ struct Tile {
   int slot, r0, n, m0;
 };
 
+// The active-expert schedule written by the routing kernels, copied to shared
+// memory once per CTA so that every role decodes tiles without global loads.
+struct Sched {
+  int n;            // active experts
+  int* tile;        // [n + 1] prefix of token chunks
+  int* slot;        // [n]
+  int* start;       // [n]
+  int* count;       // [n]
+};
+
+DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
+  Sched s;
+  s.tile = sm;
+  s.slot = sm + (kMaxE + 1);
+  s.start = sm + 2 * (kMaxE + 1);
+  s.count = sm + 3 * (kMaxE + 1);
+  int* sn = sm + 4 * (kMaxE + 1);
+  const int n = *c.n_active;
+  for (int u = threadIdx.x; u <= n; u += blockDim.x) {
+    const int tv = c.act_tile[u];
+    int sl = 0, st = 0, ct = 0;
+    if (u < n) {
+      sl = c.act_slot[u];
+      st = c.act_start[u];
+      ct = c.act_count[u];
+    }
+    s.tile[u] = tv;
+    if (u < n) {
+      s.slot[u] = sl;
+      s.start[u] = st;
+      s.count[u] = ct;
+    }
+  }
+  if (threadIdx.x == 0) *sn = n;
+  __syncthreads();
+  s.n = *sn;
+  return s;
+}
+
 // Tile t -> (active expert, token chunk, weight-row tile).  Chunks split an
 // expert's rows into ceil(count / 256) near-equal parts.
-DEV_INLINE bool get_tile(const FwdCtx& c, int t, int mtiles, Tile& out) {
-  const int nact = *c.n_active;
-  if (nact <= 0) return false;
-  const int nchunks = c.act_tile[nact];
-  if (t >= nchunks * mtiles) return false;
+DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
+  if (s.n <= 0) return false;
+  if (t >= s.tile[s.n] * mtiles) return false;
   const int mt = t % mtiles, ct = t / mtiles;
-  int lo = 0, hi = nact - 1;
-  while (lo < hi) {   // last u with act_tile[u] <= ct
+  int lo = 0, hi = s.n - 1;
+  while (lo < hi) {   // last u with tile[u] <= ct
     const int mid = (lo + hi + 1) >> 1;
-    if (c.act_tile[mid] <= ct) lo = mid;
+    if (s.tile[mid] <= ct) lo = mid;
     else hi = mid - 1;
   }
   const int u = lo;
-  const int nch = c.act_tile[u + 1] - c.act_tile[u], ch = ct - c.act_tile[u];
-  const int cnt = c.act_count[u];
+  const int nch = s.tile[u + 1] - s.tile[u], ch = ct - s.tile[u];
+  const int cnt = s.count[u];
   const int b0 = (int)((long long)ch * cnt / nch), b1 = (int)((long long)(ch + 1) * cnt / nch);
-  out.slot = c.act_slot[u];
-  out.r0 = c.act_start[u] + b0;
+  out.slot = s.slot[u];
+  out.r0 = s.start[u] + b0;
   out.n = b1 - b0;
   out.m0 = mt * kMTile;
   return true;
@@ -105,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* raw_full = bars;
-  uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* a_full = raw_empty + kStagesRaw;
+  uint64_t* raw_empty = raw_full + C::kStagesRaw;
+  uint64_t* a_full = raw_empty + C::kStagesRaw;
   uint64_t* a_empty = a_full + kStagesA;
   uint64_t* b_full = a_empty + kStagesA;
   uint64_t* b_empty = b_full + C::kStagesB;
@@ -118,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();      // routing (and, for down, h) of the preceding grids
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesRaw; ++s) {
+    for (int s = 0; s < C::kStagesRaw; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(&a_full[s], 4);
+      mbar_init(&a_full[s], kDqWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::kStagesB; ++s) {
@@ -132,16 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], 4);   // one arrive per epilogue warp
     }
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  const Sched sch = load_sched(c, reinterpret_cast<int*>(smem + C::kOffSched));   // contains __syncthreads
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -150,15 +192,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t TS = LA.tile_bytes, SB = LA.scale_bytes;
   const int nacc = GU ? 1 : 2;   // accumulator buffers (gate/up uses all 512 columns)
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == kWarpProd) {
+    // ------------------------------------------------- int4 chunk producer
     if (lane == 0) {
-      Ring rr, rb;
-      bool ok = true;
-      for (int t = blockIdx.x; ok; t += gridDim.x) {
+      Ring rr;
+      for (int t = blockIdx.x;; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(c, t, mtiles, tl)) break;
-        const int nq = (tl.n + 63) / 64;
+        if (!get_tile(sch, t, mtiles, tl)) break;
+        bool ok = true;
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&raw_empty[rr.i], rr.ph ^ 1u, c.status)) {
             ok = false;
@@ -168,6 +209,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&raw_full[rr.i], C::kRawBytes);
           tma_load_4d(dst, &tmA0, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
           if (GU) tma_load_4d(dst + 8 * 512, &tmA1, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+          rr.next(C::kStagesRaw);
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpProdB) {
+    // ------------------------------------------------- token tile producer
+    if (lane == 0) {
+      Ring rb;
+      for (int t = blockIdx.x;; t += gridDim.x) {
+        Tile tl;
+        if (!get_tile(sch, t, mtiles, tl)) break;
+        const int nq = (tl.n + 63) / 64;
+        bool ok = true;
+        for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&b_empty[rb.i], rb.ph ^ 1u, c.status)) {
             ok = false;
             break;
@@ -175,20 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* bdst = smem + C::kOffB + rb.i * C::kBBytes;
           mbar_expect_tx(&b_full[rb.i], (uint32_t)nq * 64u * 128u);
           for (int q = 0; q < nq; ++q) tma_load_2d(bdst + q * 8192, &tmB, ks * kBK, tl.r0 + q * 64, &b_full[rb.i]);
-          rr.next(kStagesRaw);
           rb.next(C::kStagesB);
         }
+        if (!ok) break;
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       Ring ra, rb, racc;
       bool ok = true;
       for (int t = blockIdx.x; ok; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(c, t, mtiles, tl)) break;
+        if (!get_tile(sch, t, mtiles, tl)) break;
         const int n16 = (tl.n + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kMTile, n16);
         if (!mbar_wait_bounded(&acc_empty[racc.i], racc.ph ^ 1u, c.status)) break;
@@ -221,54 +278,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < kDqWarps) {
     // ------------------------------------------------------------ dequant
     const int g = lane >> 2, cq = lane & 3;
     Ring rr, ra;
     bool ok = true;
     for (int t = blockIdx.x; ok; t += gridDim.x) {
       Tile tl;
-      if (!get_tile(c, t, mtiles, tl)) break;
+      if (!get_tile(sch, t, mtiles, tl)) break;
       const uint8_t* base = c.pool + (size_t)tl.slot * c.slot_bytes;
       // Scales of the thread's rows: block b in use, block b+1 prefetched.
-      __half2 slo[2][2], shi[2][2];
-      __half nlo[2][2], nhi[2][2];
-      auto load_scales = [&](int b, __half (&lo)[2][2], __half (&hi)[2][2]) {
+      __half2 slo[2][1], shi[2][1];
+      __half nlo[2][1], nhi[2][1];
+      auto load_scales = [&](int b, __half (&lo)[2][1], __half (&hi)[2][1]) {
 #pragma unroll
         for (int m = 0; m < C::kMats; ++m) {
           const MatLayout& L = (GU && m == 1) ? c.lay.up : LA;
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            const __half* sc =
-                reinterpret_cast<const __half*>(base + L.off + (size_t)(tl.m0 / 16 + warp * 2 + tt) * TS) + b * 16;
-            lo[m][tt] = sc[g];
-            hi[m][tt] = sc[g + 8];
-          }
+          const __half* sc = reinterpret_cast<const __half*>(base + L.off + (size_t)(tl.m0 / 16 + warp) * TS) + b * 16;
+          lo[m][0] = sc[g];
+          hi[m][0] = sc[g + 8];
         }
       };
       load_scales(0, nlo, nhi);
       for (int ks = 0; ks < nks; ++ks) {
         if ((ks & 3) == 0) {
 #pragma unroll
-          for (int m = 0; m < C::kMats; ++m)
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              slo[m][tt] = __half2half2(nlo[m][tt]);
-              shi[m][tt] = __half2half2(nhi[m][tt]);
-            }
+          for (int m = 0; m < C::kMats; ++m) {
+            slo[m][0] = __half2half2(nlo[m][0]);
+            shi[m][0] = __half2half2(nhi[m][0]);
+          }
           if ((ks >> 2) + 1 < (int)LA.nb) load_scales((ks >> 2) + 1, nlo, nhi);
         }
         if (!mbar_wait_bounded(&raw_full[rr.i], rr.ph, c.status)) {
           ok = false;
           break;
         }
-        uint4 q[2][2];
+        uint4 q[2][1];
         const uint8_t* raw = smem + C::kOffRaw + rr.i * C::kRawBytes;
 #pragma unroll
-        for (int m = 0; m < C::kMats; ++m)
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt)
-            q[m][tt] = *reinterpret_cast<const uint4*>(raw + (m * 8 + warp * 2 + tt) * 512 + lane * 16);
+        for (int m = 0; m < C::kMats; ++m) q[m][0] = *reinterpret_cast<const uint4*>(raw + (m * 8 + warp) * 512 + lane * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rr.i]);
         if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
@@ -279,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int m = 0; m < C::kMats; ++m) {
 #pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            const int row = (warp * 2 + tt) * 16 + g;   // and row + 8 (same swizzle phase)
+          for (int tt = 0; tt < 1; ++tt) {
+            const int row = warp * 16 + g;   // and row + 8 (same swizzle phase)
             const uint32_t rlo = abase + m * C::kAMat + row * 128 + cq * 4;
             const uint32_t rhi = rlo + 8 * 128;
             const uint32_t sw = (uint32_t)(row & 7);
@@ -300,18 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[ra.i]);
-        rr.next(kStagesRaw);
+        rr.next(C::kStagesRaw);
         ra.next(kStagesA);
       }
     }
   } else {
     // ----------------------------------------------------------- epilogue
-    const int qw = warp & 3;
+    const int qw = warp & 3;   // warps 8..11 -> TMEM lane quarters 0..3
     const int row = qw * 32 + lane;
     Ring racc;
     for (int t = blockIdx.x;; t += gridDim.x) {
       Tile tl;
-      if (!get_tile(c, t, mtiles, tl)) break;
+      if (!get_tile(sch, t, mtiles, tl)) break;
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16) + (GU ? 0u : (uint32_t)racc.i * 256u);
@@ -348,65 +396,89 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order j, FP32, then FP16.
+// A CTA covers 1024 hidden values of one token (4 per thread); the token's
+// weights (0 for an absent expert) are read once into shared memory so that
+// the y loads of all ranks are independent.
 __global__ void __launch_bounds__(256) combine_kernel(FwdCtx c) {
+  __shared__ float ws[32];
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.x;
-  const int H = c.H;
-  for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
-    float acc[8];
-    if (c.flags & 1u) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(c.x + (size_t)t * H + v * 8);
-      const __half2* xh = reinterpret_cast<const __half2*>(&xv);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(xh[i]);
-        acc[2 * i] = f.x;
-        acc[2 * i + 1] = f.y;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    }
-    for (int j = 0; j < c.k; ++j) {
-      const int p = t * c.k + j;
-      if (c.table[c.ids[p]] < 0) continue;
-      const float w = c.topw[p];
-      const float4* yp = reinterpret_cast<const float4*>(c.ybuf + (size_t)p * H + v * 8);
-      const float4 y0 = yp[0], y1 = yp[1];
-      acc[0] = fmaf(w, y0.x, acc[0]);
-      acc[1] = fmaf(w, y0.y, acc[1]);
-      acc[2] = fmaf(w, y0.z, acc[2]);
-      acc[3] = fmaf(w, y0.w, acc[3]);
-      acc[4] = fmaf(w, y1.x, acc[4]);
-      acc[5] = fmaf(w, y1.y, acc[5]);
-      acc[6] = fmaf(w, y1.z, acc[6]);
-      acc[7] = fmaf(w, y1.w, acc[7]);
-    }
-    uint4 o;
-    __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) oh[i] = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
-    *reinterpret_cast<uint4*>(c.out + (size_t)t * H + v * 8) = o;
+  const int H = c.H, k = c.k;
+  const int blocks_per_tok = (H / 4 + 255) / 256;
+  const int t = blockIdx.x / blocks_per_tok;
+  const int v = (blockIdx.x % blocks_per_tok) * 256 + threadIdx.x;   // float4 index inside the row
+  if (threadIdx.x < k) {
+    const int p = t * k + threadIdx.x;
+    ws[threadIdx.x] = c.table[c.ids[p]] >= 0 ? c.topw[p] : 0.f;
   }
+  __syncthreads();
+  if (v >= H / 4) return;
+  float acc[4];
+  if (c.flags & 1u) {
+    const uint2 xv = *reinterpret_cast<const uint2*>(c.x + (size_t)t * H + v * 4);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));
+    acc[0] = a.x;
+    acc[1] = a.y;
+    acc[2] = b.x;
+    acc[3] = b.y;
+  } else {
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+  }
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    float4 y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      y[u] = (j < k && ws[j] != 0.f) ? __ldcs(reinterpret_cast<const float4*>(c.ybuf + ((size_t)t * k + j) * H) + v)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      if (j < k && ws[j] != 0.f) {
+        const float w = ws[j];
+        acc[0] = fmaf(w, y[u].x, acc[0]);
+        acc[1] = fmaf(w, y[u].y, acc[1]);
+        acc[2] = fmaf(w, y[u].z, acc[2]);
+        acc[3] = fmaf(w, y[u].w, acc[3]);
+      }
+    }
+  }
+  uint2 o;
+  *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(acc[0], acc[1]);
+  *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(acc[2], acc[3]);
+  *reinterpret_cast<uint2*>(c.out + (size_t)t * H + v * 4) = o;
 }
 
-// xp[r] = x[sorted[r] / k]: activations in sorted-row order (one row per CTA).
+// xp[r] = x[sorted[r] / k]: activations in sorted-row order.  A CTA copies 8
+// rows; each thread keeps its 16-byte loads of all 8 rows in flight at once.
+constexpr int kGatherRows = 8;
 __global__ void __launch_bounds__(256) gather_rows_kernel(FwdCtx c) {
   pdl_wait();
   pdl_trigger();
-  const int r = blockIdx.x;
-  const int tok = c.sorted[r] / c.k;
-  const uint4* src = reinterpret_cast<const uint4*>(c.x + (size_t)tok * c.H);
-  uint4* dst = reinterpret_cast<uint4*>(c.xp + (size_t)r * c.H);
-  for (int v = threadIdx.x; v < c.H / 8; v += blockDim.x) dst[v] = __ldg(src + v);
+  const int P = c.T * c.k, vpr = c.H / 8;
+  const int r0 = blockIdx.x * kGatherRows;
+  for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+    uint4 val[kGatherRows];
+#pragma unroll
+    for (int i = 0; i < kGatherRows; ++i) {
+      const int r = r0 + i;
+      if (r < P) val[i] = __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)(c.sorted[r] / c.k) * c.H) + v);
+    }
+#pragma unroll
+    for (int i = 0; i < kGatherRows; ++i) {
+      const int r = r0 + i;
+      if (r < P) reinterpret_cast<uint4*>(c.xp + (size_t)r * c.H)[v] = val[i];
+    }
+  }
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -481,7 +553,7 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
   if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false>, Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = c.num_sms > 0 ? c.num_sms : 148;
-  e = launch_pdl(gather_rows_kernel, dim3((unsigned)P), dim3(256), 0, st, 1, c);
+  e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess)
     e = launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
                    pm.q[1]);
@@ -490,7 +562,8 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
     e = launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh, pm.q[2],
                    pm.q[2]);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
-  if (e == cudaSuccess) e = launch_pdl(combine_kernel, dim3(c.T), dim3(256), 0, st, 1, c);
+  if (e == cudaSuccess)
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }

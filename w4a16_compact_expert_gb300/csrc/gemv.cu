@@ -18,57 +18,10 @@
 // Launch chain: route -> gate/up -> down with programmatic dependent launch.
 // The down CTAs start fetching their weight tiles as soon as they are
 // resident (routing is complete by then) and wait for h only to multiply.
-#include "internal.h"
+#include "gemv_dev.cuh"
 
 namespace {
-
-constexpr int kTok = 8;   // tokens per pass (one MMA n-tile)
-
-DEV_INLINE uint32_t lds_b32_or0(const __half* p, bool valid) {
-  return valid ? *reinterpret_cast<const uint32_t*>(p) : 0u;
-}
-
-// acc[m] += tile[m] rows x B over chunks kc = kc0, kc0 + kstride, ... (< nkc).
-// B rows live in smem [np][stride] FP16; rows >= np read as zero.
-template <int NMAT>
-DEV_INLINE void mma_tiles(float (&acc)[2][4], const uint8_t* const (&tile)[2], uint32_t scale_bytes,
-                          const __half* bs, int stride, int np, int lane, int kc0, int kstride, int nkc) {
-  const int g = lane >> 2, c = lane & 3;
-  const bool brow = g < np;
-  for (int kc = kc0; kc < nkc; kc += kstride) {
-    uint4 q[NMAT];
-    __half2 slo[NMAT], shi[NMAT];
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      q[m] = *reinterpret_cast<const uint4*>(tile[m] + scale_bytes + ((size_t)kc * 32 + lane) * 16);
-      const __half* sc = reinterpret_cast<const __half*>(tile[m]) + (kc >> 2) * 16;
-      slo[m] = __half2half2(sc[g]);
-      shi[m] = __half2half2(sc[g + 8]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half* bp = bs + g * stride + kc * 64 + j * 16 + 2 * c;
-      const uint32_t b0 = lds_b32_or0(bp, brow), b1 = lds_b32_or0(bp + 8, brow);
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        const uint32_t w = j == 0 ? q[m].x : j == 1 ? q[m].y : j == 2 ? q[m].z : q[m].w;
-        uint32_t a[4];
-        dequant_word(w, slo[m], shi[m], a);
-        mma_16816(acc[m], a, b0, b1);
-      }
-    }
-  }
-}
-
-// Stage `nrows` FP16 rows (gathered by row index) into smem [*][stride].
-DEV_INLINE void stage_rows(__half* dst, int stride, int K, const __half* src, const int32_t* rows, int nrows) {
-  const int vec_per_row = K / 8;
-  for (int i = threadIdx.x; i < nrows * vec_per_row; i += blockDim.x) {
-    const int r = i / vec_per_row, v = i % vec_per_row;
-    *(reinterpret_cast<uint4*>(dst + r * stride) + v) =
-        __ldg(reinterpret_cast<const uint4*>(src + (size_t)rows[r] * K) + v);
-  }
-}
+using namespace gemv_dev;
 
 __global__ void __launch_bounds__(256) gemv_gateup_kernel(FwdCtx c, int xrows) {
   pdl_wait();      // routing results of the preceding grid
@@ -218,6 +171,7 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c, int hrows) {
   if (tid == 0) {
     unsigned last = 0;
     if (active) last = (atomicAdd(&c.down_counters[hb], 1u) == (unsigned)nact - 1u) ? 1u : 0u;
+    if (nact == 0 && u == 0) last = 1u;   // every routed expert absent: out = residual or 0
     s_last = last;
   }
   __syncthreads();
@@ -234,7 +188,7 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(FwdCtx c, int hrows) {
     }
     c.out[(size_t)t * H + hrow] = __float2half_rn(acc);
   }
-  if (tid == 0) c.down_counters[hb] = 0u;
+  if (tid == 0 && nact > 0) c.down_counters[hb] = 0u;
 }
 
 }  // namespace

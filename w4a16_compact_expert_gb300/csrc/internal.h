@@ -46,6 +46,7 @@ struct FwdCtx {
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
   unsigned* route_counter;     // [1] arrival counter (self-resetting)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
+  unsigned* grid_sync;         // [20] words of two two-level grid barriers
   DevStatus* status;
   int num_sms;
   int max_active;              // upper bound of active experts: min(E, T*k)
@@ -67,6 +68,10 @@ cudaError_t record_stage(const StageEvents& se, int i, cudaStream_t st);
 
 // gemv.cu: decode regime (gate/up kernel, then down kernel with the combine)
 cudaError_t launch_gemv_experts(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
+
+// decode_fused.cu: one cooperative launch per forward for small T
+bool fused_decode_supported(const FwdCtx& c, int max_smem);
+cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se);
 
 // gemm_tc.cu: prefill regime (gather, gate/up GEMM, down GEMM, combine)
 bool gemm_shapes_supported(int H, int I);

@@ -10,7 +10,7 @@
 // word) are cleared by each call.
 #include <mutex>
 
-#include "../../include/moe_w4a16.h"
+#include "moe_w4a16.h"
 #include "internal.h"
 
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)

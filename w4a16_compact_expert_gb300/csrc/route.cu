@@ -14,197 +14,11 @@
 //              the cluster barrier CTA 0 finishes softmax/top-k and the
 //              permutation entirely in shared memory.
 //   larger T : logits, top-k (warp per token) and permutation as three launches.
-#include <float.h>
-#include <limits.h>
-
-#include "internal.h"
+#include "route_dev.cuh"
 
 namespace {
 
-constexpr int kLogitWarps = 8;    // experts per logits CTA (one warp each)
-constexpr int kMaxEPL = 8;        // experts per lane in top-k: E <= 256
-constexpr int kMaxCluster = 8;
-constexpr unsigned kFull = 0xffffffffu;
-
-DEV_INLINE float dot8(uint4 a, uint4 b) {
-  const __half2* ha = reinterpret_cast<const __half2*>(&a);
-  const __half2* hb = reinterpret_cast<const __half2*>(&b);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fa = __half22float2(ha[i]);
-    const float2 fb = __half22float2(hb[i]);
-    s = fmaf(fa.x, fb.x, s);
-    s = fmaf(fa.y, fb.y, s);
-  }
-  return s;
-}
-
-// dot(x_t, w_e) over the whole hidden dimension (one warp).
-DEV_INLINE float warp_dot(const __half* xt, const __half* we, int H, int lane) {
-  float acc = 0.f;
-  for (int kk = lane * 8; kk < H; kk += 256)
-    acc += dot8(__ldg(reinterpret_cast<const uint4*>(xt + kk)), __ldg(reinterpret_cast<const uint4*>(we + kk)));
-  return warp_sum(acc);
-}
-
-// Softmax + top-k of one token (one warp).  lg: the token's E logits (any
-// address space), before bias and pre-norm scale r.  Writes ids/weights to
-// global memory and, when ids_s != NULL, the ids to ids_s too.
-DEV_INLINE void topk_token(const FwdCtx& c, int t, const float* lg, float r, int* ids_s) {
-  const int lane = threadIdx.x & 31;
-  const int E = c.E;
-  float v[kMaxEPL];
-  bool live[kMaxEPL];
-#pragma unroll
-  for (int i = 0; i < kMaxEPL; ++i) {
-    const int e = lane + 32 * i;
-    live[i] = e < E;
-    v[i] = live[i] ? lg[e] * r + (c.bias ? c.bias[e] : 0.f) : -INFINITY;
-  }
-  float m = -INFINITY, selv = -INFINITY;
-  int sele = 0;
-  for (int j = 0; j < c.k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i)
-      if (live[i] && (be == INT_MAX || v[i] > bv)) { bv = v[i]; be = lane + 32 * i; }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oe = __shfl_xor_sync(kFull, be, o);
-      if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
-    }
-    if (j == 0) m = bv;
-    if (lane == j) { selv = bv; sele = be; }
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i)
-      if (be == lane + 32 * i) live[i] = false;
-  }
-  float den = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxEPL; ++i)
-    if (lane + 32 * i < E && m != -INFINITY) den += expf(v[i] - m);
-  den = warp_sum(den);
-  if (lane < c.k) {
-    c.ids[(size_t)t * c.k + lane] = sele;
-    c.topw[(size_t)t * c.k + lane] = (m == -INFINITY) ? 0.f : expf(selv - m) / den;
-    if (ids_s) ids_s[t * c.k + lane] = sele;
-  }
-}
-
-DEV_INLINE float prenorm_scale(float ss, int H) { return 1.0f / sqrtf(ss / (float)H + 1e-6f); }
-
-// Stable permutation of the T*k pairs by expert (block-wide; any blockDim that
-// is a multiple of 32).  ids: the flat [T*k] expert ids (global or shared).
-// smem: nwarps*E + 2E + 1 ints.
-template <typename IdT>
-DEV_INLINE void permute_block(const FwdCtx& c, const IdT* ids, int* smem) {
-  const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = c.E, P = c.T * c.k;
-  int* hist = smem;            // [nw][E] counts, then running positions
-  int* cnt = hist + nw * E;    // [E]
-  int* off = cnt + E;          // [E+1]
-  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const int chunk = (P + nw - 1) / nw;
-  const int p_beg = min(P, w * chunk), p_end = min(P, p_beg + chunk);
-  for (int p = p_beg + lane; p < p_end; p += 32) atomicAdd(&hist[w * E + (int)ids[p]], 1);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int s = 0;
-    for (int ww = 0; ww < nw; ++ww) s += hist[ww * E + e];
-    cnt[e] = s;
-  }
-  __syncthreads();
-  if (w == 0) {   // exclusive scan of cnt: lane owns experts lane*per .. lane*per+per-1
-    const int per = (E + 31) / 32;
-    int local[kMaxEPL];
-    int s = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i) {
-      const int e = lane * per + i;
-      local[i] = s;
-      if (i < per && e < E) s += cnt[e];
-    }
-    int incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const int excl = incl - s;
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i) {
-      const int e = lane * per + i;
-      if (i < per && e < E) off[e] = excl + local[i];
-    }
-    if (lane == 31) off[E] = incl;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = off[e];
-    for (int ww = 0; ww < nw; ++ww) {
-      const int hcount = hist[ww * E + e];
-      hist[ww * E + e] = run;
-      run += hcount;
-    }
-  }
-  __syncthreads();
-  for (int base = p_beg; base < p_end; base += 32) {
-    const int p = base + lane;
-    const bool valid = p < p_end;
-    const int e = valid ? (int)ids[p] : -1 - lane;
-    const unsigned peers = __match_any_sync(kFull, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (valid) {
-      const int pos = hist[w * E + e] + rank;
-      c.sorted[pos] = p;
-      c.p2r[p] = pos;
-    }
-    __syncwarp();
-    if (valid && rank == 0) hist[w * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) c.offsets[e] = off[e];
-  if (w == 0) {   // active (routed and resident) experts in ascending order
-    int n = 0, tiles = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int ce = e < E ? cnt[e] : 0;
-      const int slot = ce > 0 ? c.table[e] : -1;
-      const bool act = ce > 0 && slot >= 0;
-      if (ce > 0 && slot < 0) {
-        atomicAdd(&c.status->miss, (unsigned long long)ce);
-        atomicOr(&c.status->flags, STATUS_MISS);
-      }
-      const unsigned am = __ballot_sync(kFull, act);
-      const int pos = n + __popc(am & ((1u << lane) - 1u));
-      const int nt = act ? (ce + c.tile_tokens - 1) / c.tile_tokens : 0;
-      int incl = nt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += x;
-      }
-      if (act) {
-        c.act_expert[pos] = e;
-        c.act_slot[pos] = slot;
-        c.act_start[pos] = off[e];
-        c.act_count[pos] = ce;
-        c.act_tile[pos] = tiles + incl - nt;
-      }
-      n += __popc(am);
-      tiles += __shfl_sync(kFull, incl, 31);
-    }
-    if (lane == 0) {
-      *c.n_active = n;
-      c.act_tile[n] = tiles;
-    }
-  }
-}
+using namespace route_dev;
 
 // ------------------------------------------------------------ small T path
 constexpr int kRouteTC = 8;       // tokens per staged x chunk
@@ -335,14 +149,27 @@ __global__ void __launch_bounds__(128) route_logits_mma_kernel(FwdCtx c) {
   const int k0 = ks * kRouteKC, kc = min(kRouteKC, H - k0);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, cq = lane & 3;
   const int vpr = kc / 8;   // 16-byte vectors per row
-  for (int i = tid; i < kRouteTile * vpr; i += blockDim.x) {
-    const int r = i / vpr, v = i % vpr;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    const int t = t0 + r, e = e0 + r;
-    *reinterpret_cast<uint4*>(xs + r * S + v * 8) =
-        t < T ? __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)t * H + k0) + v) : z;
-    *reinterpret_cast<uint4*>(ws + r * S + v * 8) =
-        e < E ? __ldg(reinterpret_cast<const uint4*>(c.router_w + (size_t)e * H + k0) + v) : z;
+  const int nvec = kRouteTile * vpr;
+  for (int i0 = 0; i0 < nvec; i0 += 8 * 128) {   // 16 independent loads in flight per thread
+    uint4 xv[8], wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 128 + tid;
+      const int r = i / vpr, v = i % vpr;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      xv[u] = (i < nvec && t0 + r < T) ? __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)(t0 + r) * H + k0) + v) : z;
+      wv[u] = (i < nvec && e0 + r < E) ? __ldg(reinterpret_cast<const uint4*>(c.router_w + (size_t)(e0 + r) * H + k0) + v)
+                                       : z;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 128 + tid;
+      if (i < nvec) {
+        const int r = i / vpr, v = i % vpr;
+        *reinterpret_cast<uint4*>(xs + r * S + v * 8) = xv[u];
+        *reinterpret_cast<uint4*>(ws + r * S + v * 8) = wv[u];
+      }
+    }
   }
   __syncthreads();
   float acc[8][4];
@@ -395,7 +222,14 @@ __global__ void __launch_bounds__(256) route_topk_kernel(FwdCtx c) {
   if (t >= c.T) return;
   for (int e = lane; e < c.E; e += 32) {
     float s = 0.f;
-    for (int ks = 0; ks < c.ksplit; ++ks) s += c.logit_part[((size_t)ks * c.T + t) * c.E + e];
+    for (int ks0 = 0; ks0 < c.ksplit; ks0 += 8) {   // 8 independent loads in flight, summed in order
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = ks0 + i < c.ksplit ? c.logit_part[((size_t)(ks0 + i) * c.T + t) * c.E + e] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += v[i];
+    }
     lg[w][e] = s;
   }
   float r = 1.f;
@@ -419,7 +253,20 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c, int ids_i
   if (ids_in_smem) {
     uint8_t* ids8 = reinterpret_cast<uint8_t*>(perm_smem);
     int* scratch = perm_smem + (P + 15) / 16 * 4;
-    for (int p = threadIdx.x; p < P; p += blockDim.x) ids8[p] = (uint8_t)c.ids[p];
+    // 16 independent loads in flight per thread before any store
+    for (int p0 = 0; p0 < P; p0 += 16 * 1024) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int p = p0 + i * 1024 + threadIdx.x;
+        v[i] = p < P ? c.ids[p] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int p = p0 + i * 1024 + threadIdx.x;
+        if (p < P) ids8[p] = (uint8_t)v[i];
+      }
+    }
     __syncthreads();
     permute_block(c, ids8, scratch);
   } else {

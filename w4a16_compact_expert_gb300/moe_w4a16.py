@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_w4a16.so")
 OK, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_PACKED, ERR_NOT_RESIDENT, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
 STATUS_NAMES = ["OK", "ERR_INVALID_ARG", "ERR_CUDA", "ERR_OOM", "ERR_NOT_PACKED", "ERR_NOT_RESIDENT",
                 "ERR_TIMEOUT", "ERR_UNSUPPORTED"]
-RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM = 1, 2, 4, 8
+RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED = 1, 2, 4, 8, 16
 
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
             "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
