@@ -45,7 +45,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--tokens", type=int, default=None, help="T per layer forward")
-    ap.add_argument("--force", choices=["auto", "gemv", "gemm"], default="auto")
+    ap.add_argument("--force", choices=["auto", "gemv", "unfused", "gemm"], default="auto",
+                    help="gemv: decode kernels (single launch when it fits); unfused: decode kernels as "
+                         "separate launches; gemm: tensor-core grouped GEMM")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=16, help="independent layers per step (16 = headline)")
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
@@ -191,7 +193,8 @@ def gpu_arm(args, rank, world, local_rank):
     T = tokens_of(args)
     steps = args.steps or (4000 if args.workload == "decode" else 100)
     warm = max(3, args.warmup)
-    force = {"auto": 0, "gemv": moe_w4a16.FORCE_GEMV, "gemm": moe_w4a16.FORCE_GEMM}[args.force]
+    force = {"auto": 0, "gemv": moe_w4a16.FORCE_GEMV, "unfused": moe_w4a16.FORCE_GEMV | moe_w4a16.UNFUSED,
+             "gemm": moe_w4a16.FORCE_GEMM}[args.force]
 
     layers, rws, xs, outs = [], [], [], []
     g = torch.Generator(device=dev)
@@ -228,6 +231,8 @@ def gpu_arm(args, rank, world, local_rank):
     for i in range(warm):
         step(i % ROTATE)
     torch.cuda.synchronize()
+    path, launches = layers[0].last_path()
+    assert all(m.last_path() == (path, launches) for m in layers)
 
     stream = torch.cuda.Stream(device=dev)
     graphs = []
@@ -287,30 +292,60 @@ def gpu_arm(args, rank, world, local_rank):
             for s in range(4):
                 stage_ms[s].append(e[s].elapsed_time(e[s + 1]))
     stage_avg = [statistics.mean(v) for v in stage_ms]
-    gemv = force == moe_w4a16.FORCE_GEMV or (force == 0 and T <= layers[0].gemv_max_tokens)
-    names = ["route", "gemv_gateup_kernel" if gemv else "gemm_gateup", "gemv_down_kernel" if gemv else "gemm_down",
-             "combine"]
     avg_u = statistics.mean(u for row in uniq for u in row)
     gate_up_bytes = 2 * (I * H // 2 + I * ((H + 255) // 256) * 2)
     down_bytes = H * I // 2 + H * ((I + 255) // 256) * 2
     P = T * K_TOP
-    kbytes = [E * H * 2 + T * H * 2,
-              avg_u * gate_up_bytes + T * H * 2 + P * I * 2,
-              avg_u * down_bytes + P * I * 2 + T * H * 2,
-              0]
-    dom = max(range(4), key=lambda s: stage_avg[s])
+    # algorithmic bytes of the three stages: router (router weight + x),
+    # gate/up (unique experts' gate+up + x + h), down (unique experts' down + h + out)
+    stage_bytes = [E * H * 2 + T * H * 2,
+                   avg_u * gate_up_bytes + T * H * 2 + P * I * 2,
+                   avg_u * down_bytes + P * I * 2 + T * H * 2]
+    layer_bytes = sum(stage_bytes)
+    layer_flops = 2.0 * P * (3 * H * I) + 2.0 * T * E * H
+    pname = moe_w4a16.PATH_NAMES[path]
+    layer_ms = ms / (steps * LAYERS)
+    if path == moe_w4a16.PATH_DECODE_FUSED:
+        # the timed graphs hold nothing but these launches, back to back: the
+        # timed region's events give the average launch duration directly
+        # (stage events inside a graph add their own gaps)
+        kern = {"fused_decode_kernel": (layer_ms, layer_bytes, layer_flops)}
+        srcs = ["decode_fused.cu", "route_dev.cuh", "gemv_dev.cuh", "common.cuh", "layout.h"]
+    elif path == moe_w4a16.PATH_DECODE:
+        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * E * H),
+                "gemv_gateup_kernel": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * H * I),
+                "gemv_down_kernel": (stage_avg[2] + stage_avg[3], stage_bytes[2], 2.0 * P * H * I)}
+        srcs = ["gemv.cu", "gemv_dev.cuh", "common.cuh", "layout.h"]
+    else:
+        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * E * H),
+                "grouped_gemm_kernel<gate_up>": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * H * I),
+                "grouped_gemm_kernel<down>": (stage_avg[2], stage_bytes[2], 2.0 * P * H * I),
+                "combine_kernel": (stage_avg[3], 0, 0.0)}
+        srcs = ["gemm_tc.cu", "common.cuh", "layout.h"]
+    dom = max(kern, key=lambda n: kern[n][0])
+    dom_ms, dom_bytes, dom_flops = kern[dom]
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except (OSError, ValueError):
         pass
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "measured" if hbm else "fallback"
-    hbm = hbm or 6800.0
-    achieved = kbytes[dom] / (stage_avg[dom] / 1e3) / 1e9
-    sha = src_hash(["gemv.cu", "common.cuh", "layout.h"] if gemv else ["gemm_tc.cu", "common.cuh", "layout.h"])
-    layer_bytes = sum(kbytes[:3])
-    layer_ms = ms / (steps * LAYERS)
+    tensor = path == moe_w4a16.PATH_GEMM
+    if tensor:
+        # FP16 dense peak = the measured BF16 cuBLAS figure (same nominal rate
+        # for FP16 and BF16 on this part); the GEMM runs inside a long step.
+        peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+        peak_src = "measured bf16_tflops_sustained (fp16 nominal = bf16)" if peak else "fallback"
+        peak = peak or 1700.0
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        unit, work = "TFLOP/s", {"algorithmic_flops_per_launch": dom_flops}
+    else:
+        peak = peaks.get("hbm_gbs")
+        peak_src = "measured hbm_gbs" if peak else "fallback"
+        peak = peak or 6800.0
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        unit, work = "GB/s", {"algorithmic_bytes_per_launch": dom_bytes}
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    sha = src_hash(srcs)
 
     # End-to-end through the C ABI with host buffers (pinned), copies timed.
     e2e_steps = max(10, min(200, steps // 10))
@@ -337,19 +372,21 @@ def gpu_arm(args, rank, world, local_rank):
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 weights x fp16 activations, fp32 accumulate", "data": "synthetic (seeded)",
         "config": workload_config(args, T) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                             "regime": "gemv" if gemv else "gemm", "cuda_graph": True},
-        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": kbytes[dom], "avg_launch_us": stage_avg[dom] * 1e3,
-                     "traffic": profiled_traffic(names[dom], T, sha)},
+                                             "path": pname, "cuda_graph": True},
+        "roofline": {"bound": "tensor" if tensor else "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "peak_source": peak_src,
+                     "avg_launch_us": dom_ms * 1e3, "traffic": profiled_traffic(dom, T, sha)} | work,
         "layer_roofline": {"algorithmic_bytes_per_layer": layer_bytes, "us_per_layer": layer_ms * 1e3,
                            "achieved_gbs": layer_bytes / (layer_ms / 1e3) / 1e9,
-                           "frac": layer_bytes / (layer_ms / 1e3) / 1e9 / hbm,
+                           "hbm_frac": layer_bytes / (layer_ms / 1e3) / 1e9 / hbm,
+                           "achieved_tflops": layer_flops / (layer_ms / 1e3) / 1e12,
                            "avg_unique_experts": avg_u},
-        "stage_us": {n: v * 1e3 for n, v in zip(names, stage_avg)},
+        "kernel_us": {n: v[0] * 1e3 for n, v in kern.items()},
+        "stage_event_us": [v * 1e3 for v in stage_avg],
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": LAYERS * T * H * 2,
                 "d2h_bytes_per_step": LAYERS * T * H * 2, "steps": e2e_steps},
-        "gpu_launches": steps * LAYERS * (3 if gemv else 4) + 0,
+        "gpu_launches": steps * LAYERS * launches,
+        "launches_per_layer_forward": launches,
         "clocks": clk.summary(peaks.get("sm_max_mhz")),
         "kernel_src": sha,
     }

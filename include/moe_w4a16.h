@@ -212,10 +212,12 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_route_noalloc(const void* x, int32_t T,
  * the caller with timing enabled), every later forward on this handle records
  * them on its stream at the stage boundaries: [0] before routing, [1] after
  * routing, [2] after the gate/up kernel, [3] after the down kernel, [4] after
- * the combine ([4] == [3] in the decode regime, whose down kernel also does
- * the combine).  While the stream is being captured they are recorded as
- * external event nodes of the graph.  NULL turns recording off.  The handle
- * keeps the five pointers, not the array. */
+ * the combine ([4] == [3] on the separate-launch decode path, whose down
+ * kernel also does the combine; on the single-launch decode path [1] == [0]
+ * and [2] == [3] == [4] bracket the one fused kernel).  While the stream is
+ * being captured they are recorded as external event nodes of the graph.
+ * NULL turns recording off.  The handle keeps the five pointers, not the
+ * array. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_set_stage_events(moe_w4a16_handle* h, void* const* events);
 
 /* Bytes of one slot row in the pool (compact weights + scales + padding). */
@@ -225,6 +227,23 @@ MOE_W4A16_API size_t moe_w4a16_slot_bytes(const moe_w4a16_handle* h);
  * larger T runs the tensor-core grouped GEMM.  Settable for sweeps. */
 MOE_W4A16_API int32_t moe_w4a16_get_gemv_max_tokens(const moe_w4a16_handle* h);
 MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h, int32_t t_star);
+
+/* Which kernel path the last successful forward on this handle enqueued, and
+ * how many kernels it launched (debug-output copies not counted):
+ *   MOE_W4A16_PATH_DECODE_FUSED  1 cooperative kernel (routing, permutation,
+ *                                gate/up, down and combine in one launch)
+ *   MOE_W4A16_PATH_DECODE        router (1 or 3 kernels) + gate/up + down
+ *   MOE_W4A16_PATH_GEMM          router (1 or 3) + gather + gate/up GEMM +
+ *                                down GEMM + combine
+ * PATH_NONE before any forward and after one with T == 0.  *launches may be
+ * NULL.  Returns -1 for a NULL handle. */
+enum {
+  MOE_W4A16_PATH_NONE = 0,
+  MOE_W4A16_PATH_DECODE_FUSED = 1,
+  MOE_W4A16_PATH_DECODE = 2,
+  MOE_W4A16_PATH_GEMM = 3
+};
+MOE_W4A16_API int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches);
 
 #ifdef __cplusplus
 }

@@ -83,3 +83,9 @@ def test_no_device_is_a_cuda_error(lib):
         pytest.skip("a GPU is present")
     st, h = _create(lib)
     assert st == moe_w4a16.ERR_CUDA and h.value is None
+
+
+def test_last_path_null_handle(lib):
+    n = ctypes.c_int32(7)
+    assert lib.moe_w4a16_last_path(None, ctypes.byref(n)) == -1
+    assert n.value == 7

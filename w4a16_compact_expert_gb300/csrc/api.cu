@@ -24,6 +24,8 @@ struct moe_w4a16_handle {
   int ksplit_fused = 1;
   int max_smem = 0;                  // opt-in shared memory per block
   int32_t gemv_max_tokens = 0;
+  int32_t last_path = 0;             // MOE_W4A16_PATH_* of the last forward
+  int32_t last_launches = 0;
   uint8_t* pool = nullptr;
   std::vector<uint8_t> packed;      // per slot: 1 once packed
   std::vector<int32_t> h_table;
@@ -392,7 +394,11 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (flags & ~31u) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "unknown flag bits");
   if ((flags & MOE_W4A16_FORCE_GEMV) && (flags & MOE_W4A16_FORCE_GEMM))
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "FORCE_GEMV and FORCE_GEMM are exclusive");
-  if (T == 0) return MOE_W4A16_OK;
+  if (T == 0) {
+    h->last_path = MOE_W4A16_PATH_NONE;
+    h->last_launches = 0;
+    return MOE_W4A16_OK;
+  }
   if (!x || !router_w || !out) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "NULL x, router_w or out");
   if (x == out) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "out must not alias x");
   if (((uintptr_t)x | (uintptr_t)router_w | (uintptr_t)out) & 15u)
@@ -422,13 +428,17 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
+  const int route_launches = fused_route && route_single_launch(c) ? 1 : 3;
+  int32_t path = gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
   if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);
   if (e == cudaSuccess) e = record_stage(h->events, 1, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   if (fused) {
     e = launch_fused_decode(c, st, h->events);
+    path = MOE_W4A16_PATH_DECODE_FUSED;
     if (e == cudaErrorNotSupported) {   // cannot be co-resident here: separate launches
+      path = MOE_W4A16_PATH_DECODE;
       e = launch_route(c, fused_route, st);
       if (e == cudaSuccess) e = launch_gemv_experts(c, st, h->events);
     }
@@ -444,7 +454,16 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (e == cudaSuccess && expert_offsets)
     e = cudaMemcpyAsync(expert_offsets, c.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug output copy");
+  h->last_path = path;
+  h->last_launches = path == MOE_W4A16_PATH_DECODE_FUSED ? 1
+                     : route_launches + (path == MOE_W4A16_PATH_GEMM ? 4 : 2);
   return MOE_W4A16_OK;
+}
+
+int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches) {
+  if (!h) return -1;
+  if (launches) *launches = h->last_launches;
+  return h->last_path;
 }
 
 moe_w4a16_status moe_w4a16_forward_host(moe_w4a16_handle* h, const void* x_host, int32_t T, const void* router_w,

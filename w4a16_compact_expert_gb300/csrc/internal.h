@@ -58,6 +58,7 @@ cudaError_t launch_repack_matrix(const uint8_t* q, const uint16_t* s, uint8_t* s
 
 // route.cu
 cudaError_t launch_route(const FwdCtx& c, bool fused, cudaStream_t st);
+bool route_single_launch(const FwdCtx& c);   // launch_route(small=true) is one kernel
 
 // Records the optional stage event `i` of a forward (no-op when unset).
 struct StageEvents {

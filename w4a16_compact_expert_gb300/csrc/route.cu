@@ -276,9 +276,11 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c, int ids_i
 
 }  // namespace
 
+bool route_single_launch(const FwdCtx& c) { return route_cluster_smem(c.T, c.E, c.H, c.k) <= 200 * 1024; }
+
 cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
   const size_t smem_small = route_cluster_smem(c.T, c.E, c.H, c.k);
-  if (small && smem_small <= 200 * 1024) {
+  if (small && route_single_launch(c)) {
     int C = (c.E + kLogitWarps - 1) / kLogitWarps;
     if (C > kMaxCluster) C = kMaxCluster;
     cudaError_t e = opt_in_smem((const void*)route_cluster_kernel, smem_small);

@@ -23,7 +23,9 @@ RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED = 1, 2, 4, 8, 16
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
             "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
             "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens",
-            "moe_w4a16_set_stage_events"]
+            "moe_w4a16_set_stage_events", "moe_w4a16_last_path"]
+PATH_NONE, PATH_DECODE_FUSED, PATH_DECODE, PATH_GEMM = 0, 1, 2, 3
+PATH_NAMES = {PATH_NONE: "none", PATH_DECODE_FUSED: "decode_fused", PATH_DECODE: "decode", PATH_GEMM: "gemm"}
 
 
 class Config(ctypes.Structure):
@@ -65,6 +67,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_get_gemv_max_tokens.restype = i32
     lib.moe_w4a16_set_gemv_max_tokens.argtypes = [vp, i32]
     lib.moe_w4a16_set_stage_events.argtypes = [vp, vp]
+    lib.moe_w4a16_last_path.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.moe_w4a16_last_path.restype = i32
     _lib = lib
     return lib
 
@@ -131,6 +135,12 @@ class MoELayer:
     @gemv_max_tokens.setter
     def gemv_max_tokens(self, v: int):
         self._check(self.lib.moe_w4a16_set_gemv_max_tokens(self.h, int(v)))
+
+    def last_path(self):
+        """(path, kernel launches) of the last forward: PATH_* and a count."""
+        n = ctypes.c_int32(0)
+        p = self.lib.moe_w4a16_last_path(self.h, ctypes.byref(n))
+        return int(p), int(n.value)
 
     # -- API
     def pack_experts(self, slot0: int, gate_q, gate_s, up_q, up_s, down_q, down_s, stream=None):
