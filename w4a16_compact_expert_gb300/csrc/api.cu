@@ -44,7 +44,7 @@ struct moe_w4a16_handle {
   __half* xp = nullptr;
   __half* hbuf = nullptr;
   float* ybuf = nullptr;
-  unsigned* counters = nullptr;      // [1 + H/32] arrival counters, then [20] grid-barrier words
+  unsigned* counters = nullptr;      // counter_words(H): grid barrier, arrival and readiness counters
   DevStatus* status = nullptr;
   uint8_t* stage = nullptr;          // pack staging for host sources
   size_t stage_bytes = 0;
@@ -223,13 +223,13 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   ALLOC(h->xp, P * H);
   ALLOC(h->hbuf, P * I);
   ALLOC(h->ybuf, P * H);
-  ALLOC(h->counters, 1 + H / 32 + 20);
+  ALLOC(h->counters, counter_words(H));
   ALLOC(h->status, 1);
   ALLOC(h->stage, h->stage_bytes);
   ALLOC(h->x_dev, T * H);
   ALLOC(h->out_dev, T * H);
 #undef ALLOC
-  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, (1 + H / 32 + 20) * sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(h->counters, 0, counter_words(H) * sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(h->d_table, 0xff, E * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -378,9 +378,9 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.xp = h->xp;
   c.hbuf = h->hbuf;
   c.ybuf = h->ybuf;
-  c.route_counter = h->counters;
-  c.down_counters = h->counters + 1;
-  c.grid_sync = h->counters + 1 + h->cfg.hidden / 32;
+  c.grid_bar = reinterpret_cast<unsigned long long*>(h->counters);
+  c.down_counters = h->counters + 2;
+  c.expert_ready = h->counters + 2 + h->cfg.hidden / 32;
   c.status = h->status;
   c.num_sms = h->num_sms;
 }
@@ -499,7 +499,7 @@ moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t* miss_count) 
   if (e != cudaSuccess) return cuda_fail(h, e, "get_status");
   if (miss_count) *miss_count = (int64_t)s.miss;
   if (s.flags & STATUS_TIMEOUT) {   // barriers and counters may be mid-use: start them afresh
-    cudaMemset(h->counters, 0, (1 + h->cfg.hidden / 32 + 20) * sizeof(unsigned));
+    cudaMemset(h->counters, 0, counter_words(h->cfg.hidden) * sizeof(unsigned));
     cudaDeviceSynchronize();
     return fail(h, MOE_W4A16_ERR_TIMEOUT, "a bounded device wait gave up");
   }

@@ -44,9 +44,11 @@ DEV_INLINE void dequant_word(uint32_t w, __half2 s_lo, __half2 s_hi, uint32_t (&
   a[3] = h2_as_u32(__hmul2(q3, s_hi));   // (row g+8, k 2c+8..+9)
 }
 
-// D += A(16x16, row) * B(16x8, col), FP16 inputs, FP32 accumulation.
+// D += A(16x16, row) * B(16x8, col), FP16 inputs, FP32 accumulation.  Not
+// volatile: a pure register operation the compiler may schedule among the
+// dequantisation arithmetic (volatile asm serialises them, about 3x slower).
 DEV_INLINE void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -5,25 +5,38 @@
 // design is not published).
 //
 // Grid = one CTA per SM, all co-resident (cooperative launch).  A CTA has 12
-// compute warps in 3 groups of 4 and one producer warp.
-//   phase 0  the grid's warps take the (token, expert, K half) dot products of
-//            the router (and per-token sums of squares for PRENORM) -> global;
-//            bounded two-level grid barrier
-//   phase 0b every CTA reads the logits and does softmax / top-k and the
-//            stable permutation itself in shared memory (CTA 0 publishes it),
-//            and stages the T token rows of x in shared memory
-//   phase 1  the CTA's share of (expert, 16-row tile) gate/up items; the
-//            producer streams their compact tiles and, right behind them, the
-//            CTA's down tiles (independent of h) through 3 bulk-copy slots;
-//            warp group q computes the items of slot q; h = SiLU(g) * u ->
-//            global (FP16); bounded grid barrier among the compute warps
-//   phase 2  the CTA's (expert, 64-row block) down items (a warp per 16-row
-//            tile, whole K, the item's h rows staged by its group) -> y (FP32);
-//            the last item to finish a 64-row block of H (arrival counter)
-//            gathers the combine in rank order.
+// compute warps in NG groups of GW (3 x 4 for T <= 8, 2 x 6 above), one
+// producer warp and one signaller warp.
+//   routing  the grid's warps take the (token, expert, K half) dot products
+//            of the router (and per-token sums of squares for PRENORM) ->
+//            global; one bounded grid barrier; then every CTA reads the logits
+//            and does softmax / top-k, the expert counts and the stable
+//            permutation in shared memory (CTA 0 publishes them).
+//   weights  a CTA owns a contiguous share of the gate/up items (expert,
+//            16-row tile of I) and of the down items (expert, 32-row block of
+//            H).  The producer warp streams them as a ring of equal entries
+//            (a gate tile, an up tile, or the two row tiles of a down item)
+//            with 1-D bulk copies, starting as soon as the active experts are
+//            known; each consumer warp releases an entry once it has read it.
+//   gate/up  group q takes items q, q + NG, ...: gate entry, then up entry,
+//            K split over the group's warps, all (<= 16) tokens of the expert
+//            at once from the x rows staged in shared memory; h = SiLU(g) * u
+//            -> global (FP16); the group leader then leaves a note for the
+//            signaller.
+//   down     once every gate/up item of its expert has counted (a bounded
+//            wait on that counter: no grid-wide barrier), the group stages the
+//            expert's h rows and multiplies its two row tiles -> y (FP32).
+//   signal   the signaller warp turns batches of gate/up notes into GPU-wide
+//            readiness counts behind one fence per batch, so no compute warp
+//            waits on a fence or an atomic.
+//   combine  a second bounded grid barrier; then the grid gathers
+//            out[t] = (x[t]) + sum_j w[t, j] y[t k + j] in rank order j.
 // Weights stay 4-bit until a warp dequantises a 16-byte chunk in registers
 // for one MMA step (FP16 operands, FP32 accumulation).  Every wait is
-// bounded: on timeout the status word records it and the CTA leaves.
+// bounded: on a timeout the status word records it, the CTA stops waiting
+// (its remaining arithmetic runs on whatever shared memory holds, and the
+// status marks the forward void), and the producer lets its copies land
+// before the CTA exits.
 #include "gemv_dev.cuh"
 #include "route_dev.cuh"
 
@@ -31,84 +44,156 @@ namespace {
 using namespace gemv_dev;
 using namespace route_dev;
 
-constexpr int kGroups = 3;                     // warp groups = ring slots
-constexpr int kGW = 4;                         // warps per group
-constexpr int kCW = kGroups * kGW;             // compute warps
-constexpr int kFThreads = (kCW + 1) * 32;      // + producer warp
-constexpr int kDownRows = 64;                  // rows of H per down item (4 tiles)
+constexpr int kCW = 12;                        // compute warps
+constexpr int kNW = kCW + 2;                   // + producer warp + signaller warp
+constexpr int kFThreads = kNW * 32;
+constexpr int kMB = 16;                        // notes per group mailbox
+constexpr int kDownRows = 32;                  // rows of H per down item (2 tiles)
 constexpr int kMaxT = 16;                      // tokens of the fused path (all staged in smem)
 constexpr int kMaxP = kMaxT * 32;
-
+constexpr int kMaxSlots = 16;                  // ring entries
+constexpr int kMinSlots = 4;
+constexpr int kMaxExperts = 256;               // readiness counters per handle
 constexpr uint32_t kSmemBudget = 226 * 1024;
 
+// warps per compute group for a batch of T tokens
+__host__ __device__ inline int fused_group_warps(int T) { return T <= 8 ? 4 : 6; }
+
 struct FusedSmem {
-  uint32_t ns, slot_bytes, off_x, x_bytes, off_red, off_route, total;
+  uint32_t ns, slot_bytes, off_x, off_h, off_red, off_sb, off_route, total;
 };
 
-// Shared memory of the fused kernel for a batch of T tokens, top-k: ns weight
-// slots (4 when they fit, else 3) feeding the 3 compute groups, the x rows /
-// per-group h rows, the cross-warp reduction buffer, and the routing state.
+// Shared memory of the fused kernel for T tokens, top-k: the ring (as many
+// entries as fit, at most kMaxSlots), the x rows [T][H + 8], per-group h rows
+// [min(T, 8)][I + 8], the cross-warp reduction buffer and the routing state.
 __host__ __device__ inline FusedSmem fused_smem(const SlotLayout& lay, int H, int I, int E, int T, int k) {
+  const int NG = kCW / fused_group_warps(T);
   FusedSmem f;
-  const uint32_t sg = 2 * lay.gate.tile_bytes, sd = (kDownRows / 16) * lay.down.tile_bytes;
+  const uint32_t sg = lay.gate.tile_bytes, sd = 2 * lay.down.tile_bytes;
   f.slot_bytes = ((sg > sd ? sg : sd) + 127) / 128 * 128;
   const int hrows = T < kTok ? T : kTok;
-  // phase 1: x [T][H + 8]; phase 2: per group h [hrows][I + 8]
-  const uint32_t xa = (uint32_t)T * (H + 8) * 2, ha = (uint32_t)kGroups * hrows * (I + 8) * 2;
-  f.x_bytes = ((xa > ha ? xa : ha) + 127) / 128 * 128;
+  const int ntok = T <= 8 ? 8 : 16;
+  const uint32_t xa = ((uint32_t)T * (H + 8) * 2 + 127) / 128 * 128;
+  const uint32_t ha = ((uint32_t)NG * hrows * (I + 8) * 2 + 127) / 128 * 128;
+  const uint32_t red = (uint32_t)kCW * 2 * 16 * ntok * 4;
+  // per-chunk sums: x rows [T][H/64], per-group h rows [min(T, 8)][I/64]
+  const uint32_t sbb = ((uint32_t)(T * (H / 64) + NG * hrows * (I / 64)) * 4 + 127) / 128 * 128;
   const int P = T * k;
   // logits [T][E] | ids, topw, sorted [P] | rnorm [T] | table, cnt, off [E + 1]
   // | active slot, start, count [E + 1] | chunk counts [ceil(P/32)][E] | misc
   const uint32_t route = (uint32_t)(T * E + 3 * P + T + 6 * (E + 1) + ((P + 31) / 32) * E + 8) * 4;
-  for (f.ns = 4; f.ns >= 3; --f.ns) {
-    f.off_x = f.ns * f.slot_bytes;
-    f.off_red = f.off_x + f.x_bytes;
-    f.off_route = f.off_red + kGroups * kGW * 2 * 16 * kTok * 4;
-    f.total = f.off_route + route;
-    if (f.total <= kSmemBudget) break;
-  }
+  const uint32_t rest = xa + ha + red + sbb + route;
+  const uint32_t ns = rest < kSmemBudget ? (kSmemBudget - rest) / f.slot_bytes : 0u;
+  f.ns = ns > (uint32_t)kMaxSlots ? (uint32_t)kMaxSlots : ns;
+  f.off_x = f.ns * f.slot_bytes;
+  f.off_h = f.off_x + xa;
+  f.off_red = f.off_h + ha;
+  f.off_sb = f.off_red + red;
+  f.off_route = f.off_sb + sbb;
+  f.total = f.off_route + route;
   return f;
 }
 
-DEV_INLINE unsigned ld_acquire(const unsigned* p) {
+DEV_INLINE unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+DEV_INLINE unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Bounded barrier over all CTAs of the grid, called by one thread per CTA.
-// Arrivals go to one of 8 sub-counters; the last arrival of a sub-counter
-// arrives on the top counter; the last top arrival resets both levels and
-// bumps the generation word the others poll.  w: [10] = 8 sub-counters,
-// top counter, generation.
-DEV_INLINE bool grid_sync_one(unsigned* w, unsigned nblocks, DevStatus* st) {
-  unsigned* gen = w + 9;
-  const unsigned g0 = ld_acquire(gen);
-  const unsigned grp = blockIdx.x & 7u;
-  const unsigned in_grp = (nblocks - grp + 7u) / 8u;   // CTAs b with b % 8 == grp
-  const unsigned ngrp = nblocks < 8u ? nblocks : 8u;
+// Bounded barrier over all CTAs of the grid, called by one thread per CTA:
+// one arrival on a monotonic 64-bit counter, then a poll until it reaches the
+// next multiple of the grid size (every launch leaves it at a multiple).
+DEV_INLINE bool grid_barrier(unsigned long long* ctr, unsigned nblocks, DevStatus* st) {
   __threadfence();
-  if (atomicAdd(&w[grp], 1u) == in_grp - 1u) {
-    w[grp] = 0u;
-    if (atomicAdd(&w[8], 1u) == ngrp - 1u) {
-      w[8] = 0u;
-      __threadfence();
-      atomicAdd(gen, 1u);
-      return true;
-    }
-  }
+  const unsigned long long old = atomicAdd(ctr, 1ull);
+  const unsigned long long target = (old / nblocks + 1ull) * nblocks;
   const long long t0 = clock64();
-  while (ld_acquire(gen) == g0) {
+  while (ld_acquire_u64(ctr) < target) {
     if (clock64() - t0 > MOE_WAIT_CYCLES) {
       atomicOr(&st->flags, STATUS_TIMEOUT);
       return false;
     }
-    __nanosleep(20);
+    __nanosleep(32);
   }
   return true;
 }
 
+// Bounded wait on an mbarrier phase that also gives up as soon as the CTA's
+// abort flag is set (by another wait that ran out); sets it on a timeout.
+DEV_INLINE bool wait_phase(uint64_t* bar, uint32_t par, volatile int* abort, DevStatus* st) {
+  if (mbar_try_wait(bar, par)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, par)) {
+    if (*abort) return false;
+    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded poll until *ctr >= target (acquire), abort-aware like wait_phase.
+DEV_INLINE bool wait_count(const unsigned* ctr, unsigned target, volatile int* abort, DevStatus* st) {
+  if (ld_acquire_u32(ctr) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_u32(ctr) < target) {
+    if (*abort) return false;
+    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Bounded wait until ring slot e % NS holds entry e (seq, written by the
+// producer once the slot is free for it) and the entry's bytes have landed.
+// Checking the entry first keeps a consumer that runs ahead from waiting on
+// a phase parity that an older, still pending phase of the slot aliases.
+// Lane 0 waits (with back-off, so waiting warps leave the issue slots to the
+// computing ones); __syncwarp then orders the other lanes' reads after it.
+DEV_INLINE void warp_wait_entry(volatile int* seq, uint64_t* full, int e, int NS, volatile int* abort,
+                                DevStatus* st, int lane) {
+  if (lane == 0) {
+    const int s = e % NS;
+    bool ok = true;
+    if (seq[s] != e) {
+      const long long t0 = clock64();
+      while (seq[s] != e) {
+        if (*abort) {
+          ok = false;
+          break;
+        }
+        if (clock64() - t0 > MOE_WAIT_CYCLES) {
+          atomicOr(&st->flags, STATUS_TIMEOUT);
+          *abort = 1;
+          ok = false;
+          break;
+        }
+        __nanosleep(40);
+      }
+    }
+    if (ok) wait_phase(&full[s], (uint32_t)((e / NS) & 1), abort, st);
+  }
+  __syncwarp();
+}
+
 DEV_INLINE void named_sync(int id, int nthreads) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory"); }
+
+DEV_INLINE void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+DEV_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Partial dot(x_t, w_e) over K in [k0, k1) (one warp, every load in flight
 // together: at most 1024 wide).
@@ -129,70 +214,158 @@ DEV_INLINE float warp_dot_part(const __half* xt, const __half* we, int k0, int k
   return warp_sum(acc);
 }
 
-// Stage rows (global, row pointers from rowptr(i)) into smem [n][stride] with
-// nthr threads (this one is t0); 4 independent 16-byte loads in flight each.
-template <typename RowFn>
-DEV_INLINE void stage(__half* dst, int stride, int K, int n, RowFn rowptr, int t0, int nthr) {
-  const int vpr = K / 8, tot = n * vpr;
-  for (int i0 = 0; i0 < tot; i0 += 4 * nthr) {
-    uint4 v[4];
+// One 64-wide K chunk of a 16-row tile against NT n-tiles of 8 tokens.
+// The int4 nibbles enter the MMA as FP16 bit patterns with no arithmetic:
+//   row g     : 1024 + u          (u = q + 8 of row g)
+//   row g + 8 : 1024 + u + 16 u'  (u' = q + 8 of row g + 8, the row-g nibble
+//                                  of the same K left in place)
+// and the chunk's exact sum over K of q * b per row follows in FP32:
+//   row g     : c0 - 1032 S       row g + 8 : (c2 - c0 - 128 S) / 16
+// with S the chunk's sum of b for that token column; times the row's block
+// scale this accumulates into acc (sum_k q s b with q s exact, FP32).
+template <int NT>
+DEV_INLINE void mma_chunk(float (&acc)[2][4], const uint4& q, float sg, float sg8, const uint4 (&bl)[NT],
+                          const uint4 (&bh)[NT], const float (&sb)[NT][2]) {
+  float c4[NT][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * nthr + t0;
-      if (i < tot) v[u] = __ldg(reinterpret_cast<const uint4*>(rowptr(i / vpr)) + i % vpr);
-    }
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * nthr + t0;
-      if (i < tot) *(reinterpret_cast<uint4*>(dst + (i / vpr) * stride) + i % vpr) = v[u];
+    for (int r = 0; r < 4; ++r) c4[nt][r] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+    uint32_t a[4];
+    a[1] = __byte_perm(w, 0x64646464u, 0x7250);   // bytes 0, 2 under exponent 0x64
+    a[3] = __byte_perm(w, 0x64646464u, 0x7351);   // bytes 1, 3
+    a[0] = a[1] & 0xFF0FFF0Fu;
+    a[2] = a[3] & 0xFF0FFF0Fu;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4& bv = j < 2 ? bl[nt] : bh[nt];
+      mma_16816(c4[nt], a, (j & 1) ? bv.z : bv.x, (j & 1) ? bv.w : bv.y);
     }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    acc[nt][0] = fmaf(sg, fmaf(-1032.f, sb[nt][0], c4[nt][0]), acc[nt][0]);
+    acc[nt][1] = fmaf(sg, fmaf(-1032.f, sb[nt][1], c4[nt][1]), acc[nt][1]);
+    acc[nt][2] = fmaf(sg8, fmaf(-128.f, sb[nt][0], c4[nt][2] - c4[nt][0]), acc[nt][2]);
+    acc[nt][3] = fmaf(sg8, fmaf(-128.f, sb[nt][1], c4[nt][3] - c4[nt][1]), acc[nt][3]);
   }
 }
 
-// acc[m] += rows of tile[m] (16 x K) x B, the lane's B row in smem (brow,
-// NULL = zero row), over chunks kc0, kc0 + kstride, ... < nkc.
-template <int NMAT>
-DEV_INLINE void mma_tiles_s(float (&acc)[2][4], const uint8_t* const (&tile)[2], uint32_t scale_bytes,
-                            const __half* brow, int lane, int kc0, int kstride, int nkc) {
+// acc[nt] += tile (16 x K) x B over the warp's K chunks kc0, kc0 + kstride,
+// ... < nkc.  brow[nt]: the lane's B row (token nt * 8 + lane / 4; any valid
+// row for columns past the tokens) in shared memory, K contiguous; sbc[nt]:
+// the per-chunk sums of the B rows of the lane's two output columns.
+template <int NT>
+DEV_INLINE void mma_fold(float (&acc)[2][4], const uint8_t* tile, uint32_t scale_bytes,
+                         const __half* const (&brow)[2], const float* const (&sbc)[2][2], int lane, int kc0,
+                         int kstride, int nkc) {
   const int g = lane >> 2, c = lane & 3;
-  for (int kc = kc0; kc < nkc; kc += kstride) {
-    uint4 q[NMAT];
-    __half2 slo[NMAT], shi[NMAT];
+  const uint8_t* qp = tile + scale_bytes + lane * 16;
+  const __half* scp = reinterpret_cast<const __half*>(tile) + g;
+  constexpr int kB = 4;   // chunks whose operands are loaded ahead together
+  int kc = kc0;
+  for (; kc + (kB - 1) * kstride < nkc; kc += kB * kstride) {
+    uint4 q[kB], bl[kB][NT], bh[kB][NT];
+    float sg[kB], sg8[kB], sb[kB][NT][2];
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      q[m] = *reinterpret_cast<const uint4*>(tile[m] + scale_bytes + ((size_t)kc * 32 + lane) * 16);
-      const __half* sc = reinterpret_cast<const __half*>(tile[m]) + (kc >> 2) * 16;
-      slo[m] = __half2half2(sc[g]);
-      shi[m] = __half2half2(sc[g + 8]);
-    }
+    for (int i = 0; i < kB; ++i) {
+      const int k2 = kc + i * kstride;
+      q[i] = *reinterpret_cast<const uint4*>(qp + (size_t)k2 * 512);
+      sg[i] = __half2float(scp[(k2 >> 2) * 16]);
+      sg8[i] = __half2float(scp[(k2 >> 2) * 16 + 8]) * 0.0625f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k0 = kc * 64 + j * 16 + 2 * c;
-      const uint32_t b0 = brow ? *reinterpret_cast<const uint32_t*>(brow + k0) : 0u;
-      const uint32_t b1 = brow ? *reinterpret_cast<const uint32_t*>(brow + k0 + 8) : 0u;
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        const uint32_t w = j == 0 ? q[m].x : j == 1 ? q[m].y : j == 2 ? q[m].z : q[m].w;
-        uint32_t a[4];
-        dequant_word(w, slo[m], shi[m], a);
-        mma_16816(acc[m], a, b0, b1);
+      for (int nt = 0; nt < NT; ++nt) {
+        bl[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + c * 16);
+        bh[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + c * 16 + 8);
+        sb[i][nt][0] = sbc[nt][0][k2];
+        sb[i][nt][1] = sbc[nt][1][k2];
       }
     }
+#pragma unroll
+    for (int i = 0; i < kB; ++i) mma_chunk<NT>(acc, q[i], sg[i], sg8[i], bl[i], bh[i], sb[i]);
+  }
+  for (; kc < nkc; kc += kstride) {
+    uint4 bl[NT], bh[NT];
+    float sb[NT][2];
+    const uint4 q = *reinterpret_cast<const uint4*>(qp + (size_t)kc * 512);
+    const float sg = __half2float(scp[(kc >> 2) * 16]);
+    const float sg8 = __half2float(scp[(kc >> 2) * 16 + 8]) * 0.0625f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      bl[nt] = *reinterpret_cast<const uint4*>(brow[nt] + kc * 64 + c * 16);
+      bh[nt] = *reinterpret_cast<const uint4*>(brow[nt] + kc * 64 + c * 16 + 8);
+      sb[nt][0] = sbc[nt][0][kc];
+      sb[nt][1] = sbc[nt][1][kc];
+    }
+    mma_chunk<NT>(acc, q, sg, sg8, bl, bh, sb);
   }
 }
 
+// Per-chunk sums of n FP16 rows [n][stride] over K (nk chunks of 64) ->
+// out[row * nk + chunk], by threads t0, t0 + nthr, ...
+DEV_INLINE void chunk_sums(float* out, const __half* rows, int stride, int n, int nk, int t0, int nthr) {
+  for (int i = t0; i < n * nk; i += nthr) {
+    const int r = i / nk, kc = i - r * nk;
+    const uint4* p = reinterpret_cast<const uint4*>(rows + (size_t)r * stride + kc * 64);
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 u = p[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[h]));
+        s += f.x + f.y;
+      }
+    }
+    out[i] = s;
+  }
+}
+
+// Group leader: posts a note (the active expert u of a finished gate/up
+// item) to the signaller.  The group barrier before the call orders the
+// item's h stores before the note.
+DEV_INLINE void post_note(int* mbox, volatile int* head, volatile int* tail, int& my_head, int v,
+                          volatile int* abort, DevStatus* st) {
+  if (my_head - *tail >= kMB) {   // mailbox full: bounded wait for the signaller
+    const long long t0 = clock64();
+    while (my_head - *tail >= kMB) {
+      if (*abort) return;
+      if (clock64() - t0 > MOE_WAIT_CYCLES) {
+        atomicOr(&st->flags, STATUS_TIMEOUT);
+        *abort = 1;
+        return;
+      }
+      __nanosleep(64);
+    }
+  }
+  mbox[my_head % kMB] = v;
+  __threadfence_block();
+  *head = ++my_head;
+}
+
+template <int GW>
 __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
+  constexpr int NG = kCW / GW;
   extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ __align__(8) uint64_t full[4], empty[4], xbar;
+  __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar;
   __shared__ int s_ok;
-  __shared__ int s_gok[kGroups];
-  __shared__ unsigned s_last[kGroups];
+  __shared__ volatile int s_abort;   // a bounded wait ran out: stop waiting
+  __shared__ volatile int s_seq[kMaxSlots];   // entry held by each ring slot
+  __shared__ int s_mbox[NG][kMB];             // group -> signaller notes
+  __shared__ volatile int s_head[NG], s_tail[NG];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const int T = c.T, E = c.E, H = c.H, I = c.I, k = c.k, P = T * k;
   const FusedSmem L = fused_smem(c.lay, H, I, E, T, k);
   __half* xcache = reinterpret_cast<__half*>(sm + L.off_x);
+  __half* hstage = reinterpret_cast<__half*>(sm + L.off_h);
   float* red = reinterpret_cast<float*>(sm + L.off_red);
+  float* sb_x = reinterpret_cast<float*>(sm + L.off_sb);        // [T][H/64]
+  float* sb_h = sb_x + T * (H / 64);                             // per group [min(T, 8)][I/64]
   float* lg = reinterpret_cast<float*>(sm + L.off_route);   // [T][E]
   int* r_ids = reinterpret_cast<int*>(lg + T * E);
   float* r_w = reinterpret_cast<float*>(r_ids + P);
@@ -210,10 +383,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   const int NS = (int)L.ns;
   if (tid == 0) {
     s_ok = 1;
+    s_abort = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], GW);   // one arrival per consumer warp
+      s_seq[s] = -1;
     }
+    for (int q = 0; q < NG; ++q) s_head[q] = s_tail[q] = 0;
     mbar_init(&xbar, 1);
     fence_mbar_init();
     // the T token rows of x, staged once (padded rows) for every gate/up item
@@ -222,12 +398,15 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     for (int t = 0; t < T; ++t) bulk_g2s(xcache + (size_t)t * (H + 8), c.x + (size_t)t * H, (uint32_t)H * 2, &xbar);
   }
   for (int e = tid; e < E; e += blockDim.x) r_table[e] = c.table[e];
+  // readiness counters start from zero: nothing counts before the routing barrier
+  if (b == 0)
+    for (int e = tid; e < E; e += blockDim.x) c.expert_ready[e] = 0u;
 
-  // ---------------------------------------------------------------- phase 0
+  // ---------------------------------------------------------------- routing
   {
     const int half = ((H / 2) + 255) / 256 * 256;   // K split point (multiple of 256)
     const int nt = 2 * T * E + ((c.flags & 2u) ? 2 * T : 0);
-    for (int task = b * (kCW + 1) + warp; task < nt; task += G * (kCW + 1)) {
+    for (int task = warp * G + b; task < nt; task += G * kNW) {
       const int part = task & 1, pair = task >> 1;
       const int k0 = part ? half : 0, k1 = part ? H : (half < H ? half : H);
       if (pair < T * E) {
@@ -243,11 +422,14 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     }
   }
   __syncthreads();
-  if (tid == 0 && !grid_sync_one(c.grid_sync, G, c.status)) s_ok = 0;
+  if (tid == 0 && !grid_barrier(c.grid_bar, (unsigned)G, c.status)) s_ok = 0;
   __syncthreads();
-  if (!s_ok) return;
+  if (!s_ok) {
+    if (tid == 0) mbar_wait_bounded(&xbar, 0, c.status);   // let the x copies land
+    return;
+  }
 
-  // --------------------------------------------------------------- phase 0b
+  // ------------------------------------------ routing in shared memory
   for (int i = tid; i < T * E; i += blockDim.x) lg[i] = __ldcg(&c.logit_part[i]) + __ldcg(&c.logit_part[T * E + i]);
   if (c.flags & 2u)
     for (int t = tid; t < T; t += blockDim.x)
@@ -258,13 +440,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     FwdCtx cl = c;   // top-k results go to shared memory
     cl.ids = r_ids;
     cl.topw = r_w;
-    for (int t = warp; t < T; t += kCW + 1)
+    for (int t = warp; t < T; t += kNW)
       topk_token(cl, t, lg + t * E, (c.flags & 2u) ? r_rnorm[t] : 1.f, nullptr);
   }
   __syncthreads();
   // counts per 32-pair chunk: __match_any_sync groups equal ids (no atomics)
   const int nchunk = (P + 31) / 32;
-  for (int ch = warp; ch < nchunk; ch += kCW + 1) {
+  for (int ch = warp; ch < nchunk; ch += kNW) {
     const int p = ch * 32 + lane;
     const int e = p < P ? r_ids[p] : -1 - lane;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -322,8 +504,98 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     if (lane == 0) r_misc[0] = n;
   }
   __syncthreads();
+  const int U = r_misc[0];
+  const int tpe1 = I / 16, tpe2 = H / kDownRows;
+  const int n1 = U * tpe1, n2 = U * tpe2;
+  const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
+  const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    // entries: 2j (gate tile) and 2j + 1 (up tile) of gate/up item j < m1,
+    // then 2 m1 + j (the 2 row tiles of down item j < m2); entry e -> slot e % NS
+    if (lane == 0) {
+      const int ne = 2 * m1 + m2;
+      int issued = 0;
+      for (int e = 0; e < ne; ++e) {
+        const int s = e % NS;
+        if (!wait_phase(&empty[s], (uint32_t)((e / NS) & 1) ^ 1u, &s_abort, c.status)) break;
+        s_seq[s] = e;
+        uint8_t* dst = sm + (size_t)s * L.slot_bytes;
+        if (e < 2 * m1) {
+          const int it = a1 + (e >> 1), u = it / tpe1, rt = it % tpe1;
+          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
+          const MatLayout& M = (e & 1) ? c.lay.up : c.lay.gate;
+          mbar_expect_tx(&full[s], M.tile_bytes);
+          bulk_g2s(dst, tile_ptr(base, M, rt), M.tile_bytes, &full[s]);
+        } else {
+          const int it = a2 + (e - 2 * m1), u = it / tpe2, hb = it % tpe2;
+          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
+          const uint32_t bytes = 2 * c.lay.down.tile_bytes;   // the 2 row tiles of a block are contiguous
+          mbar_expect_tx(&full[s], bytes);
+          bulk_g2s(dst, tile_ptr(base, c.lay.down, 2 * hb), bytes, &full[s]);
+        }
+        issued = e + 1;
+      }
+      // copies in flight land before the CTA (and its shared memory) ends:
+      // only the last entry issued into a slot can still be pending
+      for (int s = 0; s < NS && s < issued; ++s) {
+        const int last = s + (issued - 1 - s) / NS * NS;
+        mbar_wait_bounded(&full[s], (uint32_t)((last / NS) & 1), c.status);
+      }
+    }
+    return;
+  }
+
+  if (warp == kCW + 1) {
+    // ----------------------------------------------------------- signaller
+    // Turns the groups' gate/up notes into GPU-wide readiness counts, one
+    // fence per batch of notes, the adds fire-and-forget.
+    unsigned* ready = c.expert_ready;
+    int processed = 0, tails[NG];
+#pragma unroll
+    for (int q = 0; q < NG; ++q) tails[q] = 0;
+    long long t0 = clock64();
+    while (processed < m1) {
+      int heads[NG], avail = 0;
+#pragma unroll
+      for (int q = 0; q < NG; ++q) {
+        heads[q] = s_head[q];
+        avail += heads[q] - tails[q];
+      }
+      __threadfence_block();   // notes read after the heads that announce them
+      if (avail == 0) {
+        if (s_abort) break;
+        if (clock64() - t0 > MOE_WAIT_CYCLES) {
+          if (lane == 0) atomicOr(&c.status->flags, STATUS_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        __nanosleep(32);
+        continue;
+      }
+      __threadfence();   // the h stores behind these notes are visible GPU-wide before the counts
+      int n = 0;
+#pragma unroll
+      for (int q = 0; q < NG; ++q) {
+        for (; tails[q] < heads[q]; ++tails[q], ++n) {
+          const int u = reinterpret_cast<volatile int*>(s_mbox[q])[tails[q] % kMB];
+          if (lane == (n & 31)) atomicAdd(&ready[u], 1u);
+        }
+      }
+      __syncwarp();
+      if (lane == 0)
+#pragma unroll
+        for (int q = 0; q < NG; ++q) s_tail[q] = tails[q];
+      processed += n;
+      t0 = clock64();
+    }
+    return;
+  }
+
+  // -------------------------------------------------------- compute warps
   // stable scatter: rank = same-expert pairs in earlier chunks + rank inside the chunk
-  for (int ch = warp; ch < nchunk; ch += kCW + 1) {
+  for (int ch = warp; ch < nchunk; ch += kCW) {
     const int p = ch * 32 + lane;
     const int e = p < P ? r_ids[p] : -1 - lane;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -333,195 +605,183 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       r_sorted[r_off[e] + rank] = p;
     }
   }
-  __syncthreads();
-  if (tid == 0 && !mbar_wait_bounded(&xbar, 0, c.status)) s_ok = 0;
+  named_sync(1, kCW * 32);
+  if (tid == 0 && !mbar_wait_bounded(&xbar, 0, c.status)) s_abort = 1;
   if (b == 0) {   // publish the routing (debug outputs, rnorm)
-    for (int i = tid; i < P; i += blockDim.x) {
+    for (int i = tid; i < P; i += kCW * 32) {
       c.ids[i] = r_ids[i];
       c.topw[i] = r_w[i];
       c.sorted[i] = r_sorted[i];
     }
-    for (int i = tid; i <= E; i += blockDim.x) c.offsets[i] = r_off[i];
+    for (int i = tid; i <= E; i += kCW * 32) c.offsets[i] = r_off[i];
     if (c.flags & 2u)
-      for (int i = tid; i < T; i += blockDim.x) c.rnorm[i] = r_rnorm[i];
+      for (int i = tid; i < T; i += kCW * 32) c.rnorm[i] = r_rnorm[i];
   }
-
-  // --------------------------------------------------------- phases 1 and 2
-  __syncthreads();
-  if (!s_ok) return;
-  const int U = r_misc[0];
+  named_sync(1, kCW * 32);
+  chunk_sums(sb_x, xcache, H + 8, T, H / 64, tid, kCW * 32);   // x rows landed (xbar) before the barrier
+  named_sync(1, kCW * 32);
   if (U == 0) {   // every routed expert is absent: out = residual or 0
-    for (int i = b * blockDim.x + tid; i < T * H; i += G * blockDim.x)
+    for (int i = b * kCW * 32 + tid; i < T * H; i += G * kCW * 32)
       c.out[i] = (c.flags & 1u) ? c.x[i] : __float2half_rn(0.f);
     return;
   }
-  const int tpe1 = I / 16, tpe2 = H / kDownRows;
-  const int n1 = U * tpe1, n2 = U * tpe2;
-  const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
-  const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
 
-  if (warp == kCW) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      for (int j = 0; j < m1 + m2; ++j) {
-        const int s = j % NS;
-        const uint32_t par = (uint32_t)((j / NS) & 1);
-        if (!mbar_wait_bounded(&empty[s], par ^ 1u, c.status)) break;
-        uint8_t* dst = sm + (size_t)s * L.slot_bytes;
-        if (j < m1) {
-          const int it = a1 + j, u = it / tpe1, rt = it % tpe1;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const uint32_t TS = c.lay.gate.tile_bytes;
-          mbar_expect_tx(&full[s], 2 * TS);
-          bulk_g2s(dst, tile_ptr(base, c.lay.gate, rt), TS, &full[s]);
-          bulk_g2s(dst + TS, tile_ptr(base, c.lay.up, rt), TS, &full[s]);
-        } else {
-          const int it = a2 + (j - m1), u = it / tpe2, hb = it % tpe2;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const uint32_t TS = c.lay.down.tile_bytes;   // the 4 row tiles of a block are contiguous
-          mbar_expect_tx(&full[s], (kDownRows / 16) * TS);
-          bulk_g2s(dst, tile_ptr(base, c.lay.down, hb * (kDownRows / 16)), (kDownRows / 16) * TS, &full[s]);
-        }
-      }
-    }
-    return;
-  }
-
-  // ---------------------------------------------------------------- compute
-  const int q = warp / kGW, wq = warp % kGW;   // group, warp in group
-  const int gtid = tid - q * kGW * 32;         // thread index inside the group
+  const int q = warp / GW, wq = warp % GW;   // group, warp in group
+  const int gtid = tid - q * GW * 32;        // thread index inside the group
   const int g = lane >> 2, cc = lane & 3;
-  const int gbar = 2 + q;                      // named barrier of group q
-  bool ok = true;
-  // phase 1: items j = q, q + 3, ... < m1 (slot q); B = token rows of xcache
-  for (int j = q; j < m1 && ok; j += kGroups) {
-    const int s = j % NS;
-    const uint32_t par = (uint32_t)((j / NS) & 1);
-    const int it = a1 + j, u = it / tpe1, rt = it % tpe1;
-    const int start = r_astart[u], cnt = r_acount[u];
-    const uint8_t* slot = sm + (size_t)s * L.slot_bytes;
-    const uint8_t* const tiles[2] = {slot, slot + c.lay.gate.tile_bytes};
-    // one thread per group waits (bounded); the group barrier shares the outcome
-    if (gtid == 0) s_gok[q] = mbar_wait_bounded(&full[s], par, c.status) ? 1 : 0;
-    named_sync(gbar, kGW * 32);
-    if (!s_gok[q]) {
-      ok = false;
-      break;
-    }
-    float* rg = red + q * kGW * 2 * 16 * kTok;
-    for (int p0 = 0; p0 < cnt; p0 += kTok) {
-      const int np = min(kTok, cnt - p0);
-      const __half* brow = g < np ? xcache + (size_t)(r_sorted[start + p0 + g] / k) * (H + 8) : nullptr;
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      mma_tiles_s<2>(acc, tiles, c.lay.gate.scale_bytes, brow, lane, wq, kGW, H / 64);
-      float* rw = rg + wq * 2 * 16 * kTok;
+  const int gbar = 2 + q;                    // named barrier of group q
+  const int ntok = T <= 8 ? 8 : 16;
+  float* rg = red + q * GW * 2 * 16 * ntok;  // this group's reduction buffer
+  __half* hs = hstage + (size_t)q * (T < kTok ? T : kTok) * (I + 8);   // this group's h rows
+  const unsigned* ready = c.expert_ready;    // [u]: finished gate/up items of active expert u (this launch)
+  int ready_u = -1, staged_u = -1, staged_p0 = -1;
+  int my_head = 0;                           // leader: notes posted
+
+  for (int i = q; i < m1 + m2; i += NG) {
+    if (i < m1) {
+      // ---------------------------------------------------- gate/up item
+      const int it = a1 + i, u = it / tpe1, rt = it % tpe1;
+      const int start = r_astart[u], cnt = r_acount[u];   // cnt <= T <= 16
+      const int ntl = cnt > 8 ? 2 : 1;
+      const int tok0 = r_sorted[start] / k;
+      const __half* brow[2];
+      const float* sbc[2][2];
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        rw[(m * 16 + g) * kTok + 2 * cc] = acc[m][0];
-        rw[(m * 16 + g) * kTok + 2 * cc + 1] = acc[m][1];
-        rw[(m * 16 + g + 8) * kTok + 2 * cc] = acc[m][2];
-        rw[(m * 16 + g + 8) * kTok + 2 * cc + 1] = acc[m][3];
-      }
-      named_sync(gbar, kGW * 32);
-      {   // 128 threads = 16 rows x 8 tokens
-        const int row = gtid / kTok, tok = gtid % kTok;
-        if (tok < np) {
-          float gs = 0.f, us = 0.f;
+      for (int nt = 0; nt < 2; ++nt) {
+        const int ti = nt * 8 + g;   // the lane's B row; rows past cnt feed discarded columns
+        brow[nt] = xcache + (size_t)(ti < cnt ? r_sorted[start + ti] / k : tok0) * (H + 8);
 #pragma unroll
-          for (int ww = 0; ww < kGW; ++ww) {
-            gs += rg[(ww * 2 + 0) * 16 * kTok + row * kTok + tok];
-            us += rg[(ww * 2 + 1) * 16 * kTok + row * kTok + tok];
-          }
-          if (c.flags & 2u) {
-            const float r = r_rnorm[r_sorted[start + p0 + tok] / k];
-            gs *= r;
-            us *= r;
-          }
-          c.hbuf[(size_t)(start + p0 + tok) * I + rt * 16 + row] = __float2half_rn(silu_mul(gs, us));
+        for (int h = 0; h < 2; ++h) {
+          const int tc = nt * 8 + 2 * cc + h;   // the lane's output columns
+          sbc[nt][h] = sb_x + (size_t)(tc < cnt ? r_sorted[start + tc] / k : tok0) * (H / 64);
         }
       }
-      named_sync(gbar, kGW * 32);
+      float acc[2][2][4];
+#pragma unroll
+      for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[mat][nt][r] = 0.f;
+        const int e = 2 * i + mat, s = e % NS;
+        warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
+        const uint8_t* tile = sm + (size_t)s * L.slot_bytes;
+        if (ntl == 1)
+          mma_fold<1>(acc[mat], tile, c.lay.gate.scale_bytes, brow, sbc, lane, wq, GW, H / 64);
+        else
+          mma_fold<2>(acc[mat], tile, c.lay.gate.scale_bytes, brow, sbc, lane, wq, GW, H / 64);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with the entry
+      }
+      // K-split partials -> rg[warp][mat][row][token]
+      float* rw = rg + wq * 2 * 16 * ntok;
+#pragma unroll
+      for (int mat = 0; mat < 2; ++mat)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          if (nt < ntl) {
+            float* r0 = rw + (mat * 16 + g) * ntok + nt * 8 + 2 * cc;
+            r0[0] = acc[mat][nt][0];
+            r0[1] = acc[mat][nt][1];
+            r0[8 * ntok] = acc[mat][nt][2];
+            r0[8 * ntok + 1] = acc[mat][nt][3];
+          }
+      named_sync(gbar, GW * 32);
+      for (int idx = gtid; idx < 16 * cnt; idx += GW * 32) {
+        const int tok = idx >> 4, row = idx & 15;
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < GW; ++ww) {
+          gs += rg[(ww * 2 + 0) * 16 * ntok + row * ntok + tok];
+          us += rg[(ww * 2 + 1) * 16 * ntok + row * ntok + tok];
+        }
+        if (c.flags & 2u) {
+          const float r = r_rnorm[r_sorted[start + tok] / k];
+          gs *= r;
+          us *= r;
+        }
+        c.hbuf[(size_t)(start + tok) * I + rt * 16 + row] = __float2half_rn(silu_mul(gs, us));
+      }
+      named_sync(gbar, GW * 32);   // h rows written, reduction buffer free
+      if (gtid == 0) post_note(&s_mbox[q][0], &s_head[q], &s_tail[q], my_head, u, &s_abort, c.status);
+    } else {
+      // ------------------------------------------------------- down item
+      const int j2 = i - m1, it = a2 + j2, u = it / tpe2, hb = it % tpe2;
+      const int start = r_astart[u], cnt = r_acount[u];
+      const int e = 2 * m1 + j2, s = e % NS;
+      if (u != ready_u) {   // h of expert u complete (every gate/up item counted)
+        if (gtid == 0) wait_count(&ready[u], (unsigned)tpe1, &s_abort, c.status);
+        ready_u = u;
+      }
+      const int tl = wq & 1, ks = wq >> 1;   // row tile of the entry, K part
+      const uint8_t* tile = sm + (size_t)s * L.slot_bytes + (size_t)tl * c.lay.down.tile_bytes;
+      warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
+      for (int p0 = 0; p0 < cnt; p0 += kTok) {
+        const int np = min(kTok, cnt - p0);
+        float* sbg = sb_h + (size_t)q * (T < kTok ? T : kTok) * (I / 64);   // this group's h chunk sums
+        if (u != staged_u || p0 != staged_p0) {
+          named_sync(gbar, GW * 32);   // readiness seen by the leader; the group is done with hs
+          const int vpr = I / 8;       // the np rows are consecutive in hbuf
+          const __half* src = c.hbuf + (size_t)(start + p0) * I;
+          for (int v = gtid; v < np * vpr; v += GW * 32)
+            cp_async16(hs + (size_t)(v / vpr) * (I + 8) + (v % vpr) * 8, src + (size_t)v * 8);
+          cp_async_wait_all();
+          named_sync(gbar, GW * 32);
+          chunk_sums(sbg, hs, I + 8, np, I / 64, gtid, GW * 32);
+          staged_u = u;
+          staged_p0 = p0;
+        }
+        named_sync(gbar, GW * 32);   // staged rows and sums visible; previous pass done with rg
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const __half* const brow[2] = {hs + (size_t)(g < np ? g : 0) * (I + 8), hs};
+        const float* const sbc[2][2] = {{sbg + (size_t)(2 * cc < np ? 2 * cc : 0) * (I / 64),
+                                         sbg + (size_t)(2 * cc + 1 < np ? 2 * cc + 1 : 0) * (I / 64)},
+                                        {sbg, sbg}};
+        mma_fold<1>(acc, tile, c.lay.down.scale_bytes, brow, sbc, lane, ks, GW / 2, I / 64);
+        float* rw = rg + wq * 16 * kTok;
+        rw[g * kTok + 2 * cc] = acc[0][0];
+        rw[g * kTok + 2 * cc + 1] = acc[0][1];
+        rw[(g + 8) * kTok + 2 * cc] = acc[0][2];
+        rw[(g + 8) * kTok + 2 * cc + 1] = acc[0][3];
+        named_sync(gbar, GW * 32);
+        for (int idx = gtid; idx < kDownRows * np; idx += GW * 32) {
+          const int tok = idx / kDownRows, row = idx % kDownRows, t16 = row >> 4, r16 = row & 15;
+          float y = 0.f;
+#pragma unroll
+          for (int kp = 0; kp < GW / 2; ++kp) y += rg[(kp * 2 + t16) * 16 * kTok + r16 * kTok + tok];
+          c.ybuf[(size_t)r_sorted[start + p0 + tok] * H + hb * kDownRows + row] = y;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (gtid == 0) mbar_arrive(&empty[s]);
   }
-  // every CTA passes here exactly once: all h written before any down item reads it
-  __threadfence();
+
+  // ---------------------------------------------------------------- combine
+  // every y row of the layer is written once all CTAs pass this barrier;
+  // out[t] = (x[t]) + sum_j w[t, j] y[t k + j], summed in rank order j
   named_sync(1, kCW * 32);
-  if (tid == 0 && !grid_sync_one(c.grid_sync + 10, G, c.status)) s_ok = 0;
+  if (tid == 0 && !grid_barrier(c.grid_bar, (unsigned)G, c.status)) s_abort = 1;
   named_sync(1, kCW * 32);
-  if (!s_ok || !ok) return;
-  // phase 2: items j in [m1, m1 + m2) sit in slot j % 3; group q takes j % 3 == q
-  __half* hs = xcache + (size_t)q * (T < kTok ? T : kTok) * (I + 8);   // this group's h rows
-  for (int j = m1 + ((q - m1 % kGroups + kGroups) % kGroups); j < m1 + m2 && ok; j += kGroups) {
-    const int s = j % NS;
-    const uint32_t par = (uint32_t)((j / NS) & 1);
-    const int it = a2 + (j - m1), u = it / tpe2, hb = it % tpe2;
-    const int start = r_astart[u], cnt = r_acount[u];
-    const uint8_t* slot = sm + (size_t)s * L.slot_bytes;
-    const uint8_t* const tiles[2] = {slot + (size_t)wq * c.lay.down.tile_bytes, nullptr};
-    for (int p0 = 0; p0 < cnt; p0 += kTok) {
-      const int np = min(kTok, cnt - p0);
-      named_sync(gbar, kGW * 32);   // previous pass done with hs
-      stage(hs, I + 8, I, np, [&](int r) { return c.hbuf + (size_t)(start + p0 + r) * I; }, gtid, kGW * 32);
-      if (p0 == 0 && gtid == 0) s_gok[q] = mbar_wait_bounded(&full[s], par, c.status) ? 1 : 0;
-      named_sync(gbar, kGW * 32);
-      if (!s_gok[q]) {
-        ok = false;
-        break;
-      }
-      const __half* brow = g < np ? hs + (size_t)g * (I + 8) : nullptr;
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      mma_tiles_s<1>(acc, tiles, c.lay.down.scale_bytes, brow, lane, 0, 1, I / 64);
-      // accumulator (row g / g+8 of tile wq, token 2cc / 2cc+1) -> y
-      const int hrow = hb * kDownRows + wq * 16 + g;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int tok = 2 * cc + (i & 1);
-        if (tok < np) c.ybuf[(size_t)r_sorted[start + p0 + tok] * H + hrow + (i >= 2 ? 8 : 0)] = acc[0][i];
-      }
+  const bool residual = c.flags & 1u;
+  for (int idx = b * kCW * 32 + tid; idx < T * H; idx += G * kCW * 32) {
+    const int t = idx / H, hr = idx - t * H;
+    float acc = residual ? __half2float(c.x[idx]) : 0.f;
+#pragma unroll 4
+    for (int jj = 0; jj < k; ++jj) {
+      const int pp = t * k + jj;
+      if (r_table[r_ids[pp]] >= 0) acc = fmaf(r_w[pp], __ldcg(&c.ybuf[(size_t)pp * H + hr]), acc);
     }
-    if (!ok) break;
-    // the last of the U items of this 64-row block gathers the combine
-    __threadfence();
-    named_sync(gbar, kGW * 32);
-    if (gtid == 0) {
-      mbar_arrive(&empty[s]);
-      s_last[q] = (atomicAdd(&c.down_counters[hb], 1u) == (unsigned)U - 1u) ? 1u : 0u;
-    }
-    named_sync(gbar, kGW * 32);
-    if (s_last[q]) {
-      __threadfence();
-      const bool residual = c.flags & 1u;
-      for (int i = gtid; i < T * kDownRows; i += kGW * 32) {
-        const int t = i / kDownRows, hr = hb * kDownRows + (i % kDownRows);
-        float acc = residual ? __half2float(c.x[(size_t)t * H + hr]) : 0.f;
-        for (int jj = 0; jj < k; ++jj) {
-          const int p = t * k + jj;
-          if (r_table[r_ids[p]] >= 0) acc = fmaf(r_w[p], __ldcg(&c.ybuf[(size_t)p * H + hr]), acc);
-        }
-        c.out[(size_t)t * H + hr] = __float2half_rn(acc);
-      }
-      if (gtid == 0) c.down_counters[hb] = 0u;
-    }
+    c.out[idx] = __float2half_rn(acc);
   }
 }
 
-}  // namespace
-
-// The fused kernel applies to small decode batches (every token row staged
-// in shared memory) whose routing state fits next to the weight slots.
-bool fused_decode_supported(const FwdCtx& c, int max_smem) {
-  if (c.T > kMaxT || c.T * c.k > kMaxP || c.H % kDownRows || c.I % 64 || c.k > 32) return false;
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
-  return L.total <= kSmemBudget && (int)L.total <= max_smem;
-}
-
-cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
-  cudaError_t e = opt_in_smem((const void*)fused_decode_kernel, L.total);
+template <int GW>
+cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
+  cudaError_t e = opt_in_smem((const void*)fused_decode_kernel<GW>, L.total);
   if (e != cudaSuccess) return e;
   int per_sm = 0;   // all CTAs of a cooperative launch must be co-resident
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel, kFThreads, L.total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel<GW>, kFThreads, L.total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
@@ -534,7 +794,23 @@ cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEve
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, fused_decode_kernel, c);
+  return cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+}
+
+}  // namespace
+
+// The fused kernel applies to small decode batches (every token row staged
+// in shared memory) whose routing state leaves room for a ring of at least
+// kMinSlots weight entries.
+bool fused_decode_supported(const FwdCtx& c, int max_smem) {
+  if (c.T > kMaxT || c.T * c.k > kMaxP || c.H % 64 || c.I % 64 || c.k > 32 || c.E > kMaxExperts) return false;
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
+  return L.ns >= (uint32_t)kMinSlots && L.total <= kSmemBudget && (int)L.total <= max_smem;
+}
+
+cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
+  cudaError_t e = fused_group_warps(c.T) == 4 ? launch_fused<4>(c, L, st) : launch_fused<6>(c, L, st);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess) e = record_stage(se, 4, st);

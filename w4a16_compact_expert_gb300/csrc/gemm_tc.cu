@@ -134,8 +134,8 @@ DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
   return true;
 }
 
-DEV_INLINE void st_shared_b32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+DEV_INLINE void st_shared_v2_b32(uint32_t addr, uint32_t v0, uint32_t v1) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v0), "r"(v1) : "memory");
 }
 
 template <bool GU>
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int tt = 0; tt < 1; ++tt) {
             const int row = warp * 16 + g;   // and row + 8 (same swizzle phase)
-            const uint32_t rlo = abase + m * C::kAMat + row * 128 + cq * 4;
+            const uint32_t rlo = abase + m * C::kAMat + row * 128;
             const uint32_t rhi = rlo + 8 * 128;
             const uint32_t sw = (uint32_t)(row & 7);
             const uint32_t w4[4] = {q[m][tt].x, q[m][tt].y, q[m][tt].z, q[m][tt].w};
@@ -337,11 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) {
               uint32_t a[4];
               dequant_word(w4[j], slo[m][tt], shi[m][tt], a);
-              const uint32_t c0 = ((uint32_t)(2 * j) ^ sw) << 4, c1 = ((uint32_t)(2 * j + 1) ^ sw) << 4;
-              st_shared_b32(rlo + c0, a[0]);
-              st_shared_b32(rhi + c0, a[1]);
-              st_shared_b32(rlo + c1, a[2]);
-              st_shared_b32(rhi + c1, a[3]);
+              // K values cq*16 + 4j .. + 3 of the chunk: 16-byte unit 2 cq + j/2, bytes (j & 1) * 8 ..
+              const uint32_t cu = (((uint32_t)(2 * cq + (j >> 1)) ^ sw) << 4) + (uint32_t)(j & 1) * 8u;
+              st_shared_v2_b32(rlo + cu, a[0], a[2]);
+              st_shared_v2_b32(rhi + cu, a[1], a[3]);
             }
           }
         }

@@ -30,8 +30,8 @@ DEV_INLINE void mma_tiles(float (&acc)[2][4], const uint8_t* const (&tile)[2], u
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __half* bp = bs + g * stride + kc * 64 + j * 16 + 2 * c;
-      const uint32_t b0 = lds_b32_or0(bp, brow), b1 = lds_b32_or0(bp + 8, brow);
+      const __half* bp = bs + g * stride + kc * 64 + c * 16 + j * 4;   // K slots of step j (layout.h)
+      const uint32_t b0 = lds_b32_or0(bp, brow), b1 = lds_b32_or0(bp + 2, brow);
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
         const uint32_t w = j == 0 ? q[m].x : j == 1 ? q[m].y : j == 2 ? q[m].z : q[m].w;

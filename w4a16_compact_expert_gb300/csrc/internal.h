@@ -44,13 +44,19 @@ struct FwdCtx {
   __half* xp;                  // [T*k][H] activations gathered in sorted-row order (prefill)
   __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
-  unsigned* route_counter;     // [1] arrival counter (self-resetting)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
-  unsigned* grid_sync;         // [20] words of two two-level grid barriers
+  unsigned long long* grid_bar;  // grid-barrier arrivals (monotonic, a multiple of the grid between uses)
+  unsigned* expert_ready;      // [2][256] per active expert: finished gate/up items, started down items
   DevStatus* status;
   int num_sms;
   int max_active;              // upper bound of active experts: min(E, T*k)
 };
+
+// Device counter block of a handle, in 32-bit words: [0, 2) the 64-bit grid
+// barrier, [2, 2 + H/32) down arrival counters, then [2][256] per-expert
+// readiness counters.  Zero-initialised; every user leaves it zero (the grid
+// barrier: a multiple of the grid size).
+inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256; }
 
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* q, const uint16_t* s, uint8_t* slot_base,

@@ -4,16 +4,22 @@
 // It is stored as R/16 row tiles; a tile is one contiguous block of
 //   [FP16 scales: nb x 16, block-major]  then  [packed int4: nkc x 32 x 16 B]
 // (nb = ceil(K/256), nkc = K/64), so a kernel fetches a whole tile with a
-// single bulk copy.  The 16-byte chunk (kc, lane) of a tile covers K values
-// kc*64 .. kc*64+63 of rows g and g + 8 of the tile (g = lane/4, c = lane%4);
-// its word j (0..3) holds the eight values one lane owns in the A operand of
-// the 16x8x16 MMA step at K offset kc*64 + j*16:
-//   a0,a1 = (row g,   k 2c, 2c+1)   a2,a3 = (row g+8, k 2c, 2c+1)
-//   a4,a5 = (row g,   k 2c+8, +9)   a6,a7 = (row g+8, k 2c+8, +9)
-// as offset-binary nibbles u = q + 8 at nibble positions
+// single bulk copy.  The 16-byte chunk (kc, lane) of a tile holds rows g and
+// g + 8 of the tile (g = lane/4, c = lane%4) at the 16 K values
+// kc*64 + c*16 .. kc*64 + c*16 + 15.  Its word j (0..3) holds the eight values
+// the lane owns in the A operand of MMA step j (16x8x16) of the chunk, whose
+// K slots 2c, 2c+1, 2c+8, 2c+9 stand for the K values kb, kb+1, kb+2, kb+3
+// (kb = kc*64 + c*16 + 4j):
+//   a0,a1 = (row g,   kb, kb+1)     a2,a3 = (row g+8, kb, kb+1)
+//   a4,a5 = (row g,   kb+2, kb+3)   a6,a7 = (row g+8, kb+2, kb+3)
+// so a lane's B operand for the whole chunk is the 16 consecutive activation
+// values kc*64 + c*16 .. + 15 (two 16-byte loads).  Nibbles are offset binary
+// u = q + 8 at nibble positions
 //   a0->0, a2->1, a4->2, a6->3, a1->4, a3->5, a5->6, a7->7
 // so that masking with 0x000F000F / 0x00F000F0 (after a shift by 0 or 8)
-// yields the half2 pairs (a0,a1), (a2,a3), (a4,a5), (a6,a7).
+// yields the half2 pairs (a0,a1), (a2,a3), (a4,a5), (a6,a7), and the bytes
+// 0, 2 (1, 3) of a word are the (row g, row g+8) nibble pairs of (a0..a3)
+// ((a4..a7)).
 #pragma once
 #include <stddef.h>
 #include <stdint.h>

@@ -19,11 +19,11 @@ __global__ void repack_q_kernel(const uint8_t* __restrict__ q, uint8_t* __restri
     const int kc = in_tile >> 7;
     const int g = lane >> 2, c = lane & 3;
     const int r_lo = rt * 16 + g, r_hi = r_lo + 8;
-    const int kb = kc * 64 + j * 16 + 2 * c;            // even
+    const int kb = kc * 64 + c * 16 + j * 4;            // K of (a0, a1); (a4, a5) follow at kb + 2
     const uint32_t b_lo0 = q[(size_t)r_lo * half_k + kb / 2];        // (a0, a1)
     const uint32_t b_hi0 = q[(size_t)r_hi * half_k + kb / 2];        // (a2, a3)
-    const uint32_t b_lo8 = q[(size_t)r_lo * half_k + (kb + 8) / 2];  // (a4, a5)
-    const uint32_t b_hi8 = q[(size_t)r_hi * half_k + (kb + 8) / 2];  // (a6, a7)
+    const uint32_t b_lo8 = q[(size_t)r_lo * half_k + (kb + 2) / 2];  // (a4, a5)
+    const uint32_t b_hi8 = q[(size_t)r_hi * half_k + (kb + 2) / 2];  // (a6, a7)
     uint32_t w = (b_lo0 & 15u) | ((b_hi0 & 15u) << 4) | ((b_lo8 & 15u) << 8) | ((b_hi8 & 15u) << 12) |
                  ((b_lo0 >> 4) << 16) | ((b_hi0 >> 4) << 20) | ((b_lo8 >> 4) << 24) | ((b_hi8 >> 4) << 28);
     uint32_t* dst = reinterpret_cast<uint32_t*>(mat + (size_t)rt * m.tile_bytes + m.scale_bytes) + in_tile;
