@@ -1,15 +1,25 @@
 #!/usr/bin/env python3
 """Throughput of the W4A16 routed-expert MoE layer on one GB300 (per rank).
 
-Workload (default, "decode"): 16 independent OLMoE-shaped MoE layers
-(H=2048, I=1024, E=64, top-8, all experts resident), each run on its own batch
-of T decode tokens.  One step = one forward of each of the 16 layers, i.e. the
-whole hot path (router top-k, permutation, gate/up with in-kernel int4
-dequantisation, SiLU*up, down, top-k combine) 16 times over 3.27 GB of
-distinct packed weights, so every step streams its experts from HBM (the
-touched weights of a step exceed the 129 MB L2).  The activations rotate over
-8 seeded batches per layer.  Metric: MoE-layer tokens/s = 16 * T * steps /
-time.  "prefill" runs the same stack at T = 2048.
+Workloads (--workload):
+  decode   (default) 16 independent OLMoE-shaped layers (H=2048, I=1024,
+           E=64, top-8, all experts resident), each run on its own batch of T
+           decode tokens (default T=4).  One step = one forward of each layer:
+           the whole hot path (router top-k, permutation, gate/up with in-kernel
+           int4 dequantisation, SiLU*up, down, top-k combine) 16 times over
+           3.27 GB of distinct packed weights, so every step streams its experts
+           from HBM (more than the 129 MB L2).  Activations rotate over 8 seeded
+           batches per layer.
+  prefill  the same 16 layers at T=2048 (--variant 2: per-expert logit bias
+           ~ N(0, 1), a skewed expert load).
+  qwen     8 independent Qwen-MoE-shaped partial-residency pools (H=2048,
+           I=1408, E=60, top-4, 39 resident experts at permuted slots, -inf
+           logit bias for the 21 absent ones; 1.37 GB), default T=8.
+  stack    16 OLMoE-shaped layers run in sequence, x <- x + MoE(rmsnorm(x)),
+           T tokens; --sweep times T in {1, 8, 64, 512, 2048} with the decode
+           kernels and the grouped GEMM forced in turn and reports the
+           crossover.
+Metric: MoE-layer tokens/s = layers * T * steps / time.
 
 Prints ONE JSON line (rank 0).  --impl reference times the float64 CPU oracle
 on the same workload instead (bounded sample, host cores).
@@ -29,12 +39,24 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "MoE-layer tokens/s (OLMoE-shaped W4A16 layer, packed-weight HBM roofline)"
+METRIC = "MoE-layer tokens/s (W4A16 routed-expert layer; packed-weight HBM roofline for decode, FP16 tensor roofline for prefill)"
 UNIT = "tokens/s"
-H, I, E, K_TOP = 2048, 1024, 64, 8
-EXPERT_BYTES = 3_194_880
-LAYERS = 16
 ROTATE = 8
+
+
+class Shape:
+    def __init__(self, name, H, I, E, k, slots):
+        self.name, self.H, self.I, self.E, self.k, self.slots = name, H, I, E, k, slots
+        self.nb_h = (H + 255) // 256
+        self.nb_i = (I + 255) // 256
+        self.gate_up_bytes = 2 * (I * H // 2 + I * self.nb_h * 2)
+        self.down_bytes = H * I // 2 + H * self.nb_i * 2
+        self.expert_bytes = self.gate_up_bytes + self.down_bytes
+
+
+OLMOE = Shape("OLMoE", 2048, 1024, 64, 8, 64)
+QWEN = Shape("Qwen-MoE", 2048, 1408, 60, 4, 39)
+SWEEP_T = [1, 8, 64, 512, 2048]
 
 
 def parse():
@@ -43,50 +65,84 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "prefill", "qwen", "stack"], default="decode")
+    ap.add_argument("--variant", type=int, default=1, help="prefill: 1 = no bias, 2 = logit bias ~ N(0, 1)")
     ap.add_argument("--tokens", type=int, default=None, help="T per layer forward")
     ap.add_argument("--force", choices=["auto", "gemv", "unfused", "gemm"], default="auto",
                     help="gemv: decode kernels (single launch when it fits); unfused: decode kernels as "
                          "separate launches; gemm: tensor-core grouped GEMM")
+    ap.add_argument("--sweep", action="store_true", help="stack: T sweep with both kernel families")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--layers", type=int, default=16, help="independent layers per step (16 = headline)")
+    ap.add_argument("--layers", type=int, default=None, help="layers (pools) per step")
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-max-steps", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
+def shape_of(args):
+    return QWEN if args.workload == "qwen" else OLMOE
+
+
 def tokens_of(args) -> int:
     if args.tokens:
         return args.tokens
-    return 4 if args.workload == "decode" else 2048
+    return {"decode": 4, "prefill": 2048, "qwen": 8, "stack": 8}[args.workload]
+
+
+def layers_of(args) -> int:
+    if args.layers:
+        return args.layers
+    return 8 if args.workload == "qwen" else 16
+
+
+def flags_of(args) -> int:
+    from w4a16_compact_expert_gb300 import moe_w4a16 as M
+    return (M.RESIDUAL | M.PRENORM) if args.workload == "stack" else 0
 
 
 def workload_config(args, T):
-    global LAYERS
-    LAYERS = args.layers
-    return {"workload": f"OLMoE-shaped W4A16 MoE layer ({args.workload}), H={H} I={I} E={E} top-{K_TOP}, "
-                        f"T={T} tokens per layer forward, {LAYERS} independent layers per step",
-            "tokens_per_layer": T, "layers_per_step": LAYERS, "hidden": H, "inter": I, "experts": E, "top_k": K_TOP,
-            "weights": "int4 qpacked, 256-value blocks, FP16 scales; all experts resident",
-            "l2": "inputs larger than L2: 3.27 GB of distinct packed weights per step rotation",
+    s, L = shape_of(args), layers_of(args)
+    desc = {
+        "decode": f"{L} independent OLMoE-shaped W4A16 MoE layers, decode batch",
+        "prefill": f"{L} independent OLMoE-shaped W4A16 MoE layers, prefill batch"
+                   + (", per-expert logit bias ~ N(0,1)" if args.variant == 2 else ""),
+        "qwen": f"{L} independent Qwen-MoE-shaped partial-residency pools ({s.slots} of {s.E} experts resident "
+                f"at permuted slots, -inf bias for absent)",
+        "stack": f"{L} OLMoE-shaped W4A16 MoE layers in sequence, x <- x + MoE(rmsnorm(x))",
+    }[args.workload]
+    total = L * s.slots * s.expert_bytes
+    return {"workload": f"{desc}: H={s.H} I={s.I} E={s.E} top-{s.k}, T={T} tokens per layer forward",
+            "tokens_per_layer": T, "layers_per_step": L, "hidden": s.H, "inter": s.I, "experts": s.E,
+            "top_k": s.k, "resident_slots": s.slots,
+            "weights": "int4 qpacked, 256-value blocks, FP16 scales",
+            "l2": f"inputs larger than L2: {total / 1e9:.2f} GB of distinct packed weights per step",
             "activation_rotation": ROTATE}
 
 
 # ------------------------------------------------------------ CPU oracle leg
 
 def cpu_leg(args):
-    """Times the float64 oracle (as it stands) on one OLMoE layer at T tokens."""
-    import numpy as np  # noqa: F401
+    """Times the float64 oracle (as it stands) on single layers of the workload."""
     from oracle import moe_oracle
     from w4a16_compact_expert_gb300 import synth
     T = tokens_of(args)
-    layer = synth.olmoe_decode_layer()
-    xs = [synth.draw_x(synth.SEED_OLMOE_DECODE + r, T, H) for r in range(ROTATE)]
-    arrays = layer.experts.arrays()
+    if args.workload == "qwen":
+        layer = synth.qwen_partial_layer()
+        seed = synth.SEED_QWEN_PARTIAL
+    elif args.workload == "prefill":
+        layer = synth.olmoe_prefill_layer(args.variant)
+        seed = synth.SEED_OLMOE_PREFILL
+    else:
+        layer = synth.olmoe_decode_layer()
+        seed = synth.SEED_OLMOE_DECODE
+    flags = (moe_oracle.FLAG_RESIDUAL | moe_oracle.FLAG_PRENORM) if args.workload == "stack" else 0
+    xs = [synth.draw_x(seed + r, T, layer.shape.hidden) for r in range(ROTATE)]
+    experts = layer.slot_experts().arrays()
     done, t0 = 0, time.perf_counter()
     while True:
-        moe_oracle.moe_layer(xs[done % ROTATE], layer.router_w, layer.bias, arrays, K_TOP)
+        moe_oracle.moe_layer(xs[done % ROTATE], layer.router_w, layer.bias, experts, layer.shape.top_k, flags,
+                             layer.expert_to_slot)
         done += 1
         el = time.perf_counter() - t0
         if el >= args.cpu_seconds or (args.cpu_max_steps and done >= args.cpu_max_steps):
@@ -97,11 +153,18 @@ def cpu_leg(args):
 def run_cpu_leg(args, seconds, max_steps=0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-leg", "--workload", args.workload,
-           "--tokens", str(tokens_of(args)), "--cpu-seconds", str(seconds), "--cpu-max-steps", str(max_steps)]
+           "--variant", str(args.variant), "--tokens", str(tokens_of(args)), "--cpu-seconds", str(seconds),
+           "--cpu-max-steps", str(max_steps)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 4 + 300)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_sample_text(args, leg):
+    T = tokens_of(args)
+    return (f"{leg['steps']} float64-oracle forwards of one {shape_of(args).name}-shaped layer at T={T} "
+            f"in {leg['seconds']:.1f} s, 1 thread")
 
 
 # ------------------------------------------------------------------ clocks
@@ -181,71 +244,107 @@ def profiled_traffic(kernel, tokens, sha):
     return None
 
 
-def gpu_arm(args, rank, world, local_rank):
-    import torch
-    global LAYERS
-    LAYERS = args.layers
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
 
-    from w4a16_compact_expert_gb300 import build_ext, moe_w4a16, synth
-    build_ext.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    T = tokens_of(args)
-    steps = args.steps or (4000 if args.workload == "decode" else 100)
-    warm = max(3, args.warmup)
-    force = {"auto": 0, "gemv": moe_w4a16.FORCE_GEMV, "unfused": moe_w4a16.FORCE_GEMV | moe_w4a16.UNFUSED,
-             "gemm": moe_w4a16.FORCE_GEMM}[args.force]
 
-    layers, rws, xs, outs = [], [], [], []
-    g = torch.Generator(device=dev)
-    for l in range(LAYERS):
-        m = moe_w4a16.MoELayer(H, I, E, K_TOP, max_tokens=T, device=local_rank)
-        ex = synth.device_random_experts(synth.OLMOE, E, seed=synth.SEED_OLMOE_STACK * 1000 + l, device=dev)
-        m.pack_experts(0, *ex)
-        m.set_slot_table(list(range(E)))
-        del ex
-        g.manual_seed(10_000 + l)
-        rws.append((torch.randn(E, H, device=dev, generator=g) * 0.02).half())
-        xs.append([torch.randn(T, H, device=dev, generator=g).half() for _ in range(ROTATE)])
-        outs.append(torch.empty(T, H, device=dev, dtype=torch.float16))
-        layers.append(m)
-    torch.cuda.synchronize()
+class Workload:
+    """The device-resident layers of one run: handles, router weights, biases,
+    the rotating activations and the output buffers."""
 
-    # Unique experts actually routed per (layer, batch): algorithmic bytes.
-    uniq = [[0] * ROTATE for _ in range(LAYERS)]
-    for l, m in enumerate(layers):
-        for r in range(ROTATE):
-            _, dbg = m.forward(xs[l][r], rws[l], None, force, out=outs[l], debug=True)
-            uniq[l][r] = int(torch.unique(dbg["ids"]).numel())
-    torch.cuda.synchronize()
-    for m in layers:
-        st, miss = m.get_status()
-        assert st == moe_w4a16.OK and miss == 0
+    def __init__(self, args, T, dev, local_rank):
+        import numpy as np
+        import torch
+        from w4a16_compact_expert_gb300 import moe_w4a16, synth
+        s = shape_of(args)
+        self.shape, self.T, self.L = s, T, layers_of(args)
+        self.chain = args.workload == "stack"
+        self.flags = flags_of(args)
+        self.layers, self.rws, self.biases = [], [], []
+        g = torch.Generator(device=dev)
+        base_seed = synth.SEED_QWEN_PARTIAL if s is QWEN else synth.SEED_OLMOE_STACK
+        for l in range(self.L):
+            m = moe_w4a16.MoELayer(s.H, s.I, s.E, s.k, num_slots=s.slots, max_tokens=T, device=local_rank)
+            ex = synth.device_random_experts(synth.QWEN if s is QWEN else synth.OLMOE, s.slots,
+                                             seed=base_seed * 1000 + l, device=dev)
+            m.pack_experts(0, *ex)
+            del ex
+            g.manual_seed(10_000 + l)
+            self.rws.append((torch.randn(s.E, s.H, device=dev, generator=g) * 0.02).half())
+            if s.slots < s.E:
+                # seeded resident subset at a seeded permutation of the slots; -inf bias for the rest
+                rng = np.random.Generator(np.random.PCG64(base_seed * 1000 + l))
+                resident = np.sort(rng.choice(s.E, s.slots, replace=False))
+                slots = rng.permutation(s.slots)
+                table = np.full(s.E, -1, dtype=np.int32)
+                table[resident] = slots
+                bias = np.where(table >= 0, 0.0, -np.inf).astype(np.float32)
+                m.set_slot_table(table.tolist())
+                self.biases.append(torch.from_numpy(bias).to(dev))
+            else:
+                m.set_slot_table(list(range(s.E)))
+                if args.workload == "prefill" and args.variant == 2:
+                    self.biases.append(torch.randn(s.E, device=dev, generator=g).float())
+                else:
+                    self.biases.append(None)
+            self.layers.append(m)
+        g.manual_seed(20_000)
+        if self.chain:
+            self.xs = [torch.randn(T, s.H, device=dev, generator=g).half() for _ in range(ROTATE)]
+            self.bufs = [torch.empty(T, s.H, device=dev, dtype=torch.float16) for _ in range(2)]
+        else:
+            self.xs = [[torch.randn(T, s.H, device=dev, generator=g).half() for _ in range(ROTATE)]
+                       for _ in range(self.L)]
+            self.outs = [torch.empty(T, s.H, device=dev, dtype=torch.float16) for _ in range(self.L)]
+        torch.cuda.synchronize()
 
-    def step(r, events=None):
-        for l, m in enumerate(layers):
+    def _io(self, l, r):
+        if self.chain:
+            return (self.xs[r] if l == 0 else self.bufs[(l - 1) % 2]), self.bufs[l % 2]
+        return self.xs[l][r], self.outs[l]
+
+    def step(self, r, force, events=None):
+        for l, m in enumerate(self.layers):
             if events is not None:
                 m.set_stage_events(events[l])
-            m.forward(xs[l][r], rws[l], None, force, out=outs[l])
+            x, out = self._io(l, r)
+            m.forward(x, self.rws[l], self.biases[l], self.flags | force, out=out)
 
+    def unique_experts(self, force):
+        """Mean number of distinct routed experts per layer forward (from the actual routing)."""
+        import torch
+        n = []
+        for r in range(ROTATE):
+            for l, m in enumerate(self.layers):
+                x, out = self._io(l, r)
+                _, dbg = m.forward(x, self.rws[l], self.biases[l], self.flags | force, out=out, debug=True)
+                n.append(int(torch.unique(dbg["ids"]).numel()))
+        torch.cuda.synchronize()
+        return statistics.mean(n)
+
+    def close(self):
+        for m in self.layers:
+            m.close()
+
+
+def time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks):
+    import torch
     for i in range(warm):
-        step(i % ROTATE)
+        wl.step(i % ROTATE, force)
     torch.cuda.synchronize()
-    path, launches = layers[0].last_path()
-    assert all(m.last_path() == (path, launches) for m in layers)
-
-    stream = torch.cuda.Stream(device=dev)
     graphs = []
     with torch.cuda.stream(stream):
         for r in range(ROTATE):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=stream):
-                step(r)
+                wl.step(r, force)
             graphs.append(gr)
     for gr in graphs:
         gr.replay()
     torch.cuda.synchronize()
-
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -261,15 +360,16 @@ def gpu_arm(args, rank, world, local_rank):
         torch.distributed.barrier()
     ms = ev0.elapsed_time(ev1)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
+        t = torch.tensor([ms], device=torch.device("cuda", local_rank))
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    tokens_total = LAYERS * T * steps * world
-    value = tokens_total / (ms / 1e3)
+    return ms, clk.summary(peaks.get("sm_max_mhz"))
 
-    # Per-kernel durations: the same steps captured with stage events.
-    prof_steps = ROTATE
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(LAYERS)] for _ in range(prof_steps)]
+
+def stage_times(wl, force, stream):
+    """Per-stage durations from one more capture of the same steps with stage events."""
+    import torch
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(wl.L)] for _ in range(ROTATE)]
     for row in evs:
         for per_layer in row:
             for e in per_layer:
@@ -278,121 +378,193 @@ def gpu_arm(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         gp = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gp, stream=stream):
-            for r in range(prof_steps):
-                step(r, evs[r])
-        for m in layers:
+            for r in range(ROTATE):
+                wl.step(r, force, evs[r])
+        for m in wl.layers:
             m.set_stage_events(None)
         gp.replay()
         gp.replay()
     torch.cuda.synchronize()
     stage_ms = [[], [], [], []]
-    for r in range(prof_steps):
-        for l in range(LAYERS):
+    for r in range(ROTATE):
+        for l in range(wl.L):
             e = evs[r][l]
             for s in range(4):
                 stage_ms[s].append(e[s].elapsed_time(e[s + 1]))
-    stage_avg = [statistics.mean(v) for v in stage_ms]
-    avg_u = statistics.mean(u for row in uniq for u in row)
-    gate_up_bytes = 2 * (I * H // 2 + I * ((H + 255) // 256) * 2)
-    down_bytes = H * I // 2 + H * ((I + 255) // 256) * 2
-    P = T * K_TOP
-    # algorithmic bytes of the three stages: router (router weight + x),
-    # gate/up (unique experts' gate+up + x + h), down (unique experts' down + h + out)
-    stage_bytes = [E * H * 2 + T * H * 2,
-                   avg_u * gate_up_bytes + T * H * 2 + P * I * 2,
-                   avg_u * down_bytes + P * I * 2 + T * H * 2]
+    return [statistics.mean(v) for v in stage_ms]
+
+
+def e2e_rate(wl, force, steps, world, local_rank):
+    """Same metric through forward_host: pinned host x in, host out, copies timed."""
+    import torch
+    T, H = wl.T, wl.shape.H
+    if wl.chain:
+        xh = [wl.xs[r].cpu().pin_memory() for r in range(ROTATE)]
+    else:
+        xh = [[wl.xs[l][r].cpu().pin_memory() for r in range(ROTATE)] for l in range(wl.L)]
+    oh = [torch.empty(T, H, dtype=torch.float16).pin_memory() for _ in range(2 if wl.chain else wl.L)]
+
+    def one(i):
+        for l, m in enumerate(wl.layers):
+            if wl.chain:
+                src = xh[i % ROTATE] if l == 0 else oh[(l - 1) % 2]
+                m.forward_host(src, wl.rws[l], wl.biases[l], wl.flags | force, out_host=oh[l % 2])
+            else:
+                m.forward_host(xh[l][i % ROTATE], wl.rws[l], wl.biases[l], wl.flags | force, out_host=oh[l])
+
+    for i in range(2):
+        one(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    el = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([el], device=torch.device("cuda", local_rank))
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        el = float(t.item())
+    return wl.L * T * steps * world / el
+
+
+def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
+    from w4a16_compact_expert_gb300 import moe_w4a16 as M
+    s, T = wl.shape, wl.T
+    P = T * s.k
+    stage_bytes = [s.E * s.H * 2 + T * s.H * 2,
+                   avg_u * s.gate_up_bytes + T * s.H * 2 + P * s.I * 2,
+                   avg_u * s.down_bytes + P * s.I * 2 + T * s.H * 2]
     layer_bytes = sum(stage_bytes)
-    layer_flops = 2.0 * P * (3 * H * I) + 2.0 * T * E * H
-    pname = moe_w4a16.PATH_NAMES[path]
-    layer_ms = ms / (steps * LAYERS)
-    if path == moe_w4a16.PATH_DECODE_FUSED:
+    layer_flops = 2.0 * P * (3 * s.H * s.I) + 2.0 * T * s.E * s.H
+    if path == M.PATH_DECODE_FUSED:
         # the timed graphs hold nothing but these launches, back to back: the
         # timed region's events give the average launch duration directly
-        # (stage events inside a graph add their own gaps)
         kern = {"fused_decode_kernel": (layer_ms, layer_bytes, layer_flops)}
         srcs = ["decode_fused.cu", "route_dev.cuh", "gemv_dev.cuh", "common.cuh", "layout.h"]
-    elif path == moe_w4a16.PATH_DECODE:
-        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * E * H),
-                "gemv_gateup_kernel": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * H * I),
-                "gemv_down_kernel": (stage_avg[2] + stage_avg[3], stage_bytes[2], 2.0 * P * H * I)}
+    elif path == M.PATH_DECODE:
+        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * s.E * s.H),
+                "gemv_gateup_kernel": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * s.H * s.I),
+                "gemv_down_kernel": (stage_avg[2] + stage_avg[3], stage_bytes[2], 2.0 * P * s.H * s.I)}
         srcs = ["gemv.cu", "gemv_dev.cuh", "common.cuh", "layout.h"]
     else:
-        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * E * H),
-                "grouped_gemm_kernel<gate_up>": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * H * I),
-                "grouped_gemm_kernel<down>": (stage_avg[2], stage_bytes[2], 2.0 * P * H * I),
+        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * s.E * s.H),
+                "grouped_gemm_kernel<gate_up>": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * s.H * s.I),
+                "grouped_gemm_kernel<down>": (stage_avg[2], stage_bytes[2], 2.0 * P * s.H * s.I),
                 "combine_kernel": (stage_avg[3], 0, 0.0)}
         srcs = ["gemm_tc.cu", "common.cuh", "layout.h"]
     dom = max(kern, key=lambda n: kern[n][0])
     dom_ms, dom_bytes, dom_flops = kern[dom]
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except (OSError, ValueError):
-        pass
-    tensor = path == moe_w4a16.PATH_GEMM
+    tensor = path == M.PATH_GEMM
+    hbm = peaks.get("hbm_gbs") or 6800.0
     if tensor:
         # FP16 dense peak = the measured BF16 cuBLAS figure (same nominal rate
         # for FP16 and BF16 on this part); the GEMM runs inside a long step.
         peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
-        peak_src = "measured bf16_tflops_sustained (fp16 nominal = bf16)" if peak else "fallback"
+        src = "measured bf16_tflops_sustained (fp16 nominal = bf16)" if peak else "fallback"
         peak = peak or 1700.0
         achieved = dom_flops / (dom_ms / 1e3) / 1e12
         unit, work = "TFLOP/s", {"algorithmic_flops_per_launch": dom_flops}
     else:
         peak = peaks.get("hbm_gbs")
-        peak_src = "measured hbm_gbs" if peak else "fallback"
+        src = "measured hbm_gbs" if peak else "fallback"
         peak = peak or 6800.0
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         unit, work = "GB/s", {"algorithmic_bytes_per_launch": dom_bytes}
-    hbm = peaks.get("hbm_gbs") or 6800.0
     sha = src_hash(srcs)
+    roof = {"bound": "tensor" if tensor else "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+            "unit": unit, "frac": achieved / peak, "peak_source": src, "avg_launch_us": dom_ms * 1e3,
+            "traffic": profiled_traffic(dom, T, sha)} | work
+    layer = {"algorithmic_bytes_per_layer": layer_bytes, "us_per_layer": layer_ms * 1e3,
+             "achieved_gbs": layer_bytes / (layer_ms / 1e3) / 1e9,
+             "hbm_frac": layer_bytes / (layer_ms / 1e3) / 1e9 / hbm,
+             "achieved_tflops": layer_flops / (layer_ms / 1e3) / 1e12, "avg_unique_experts": avg_u}
+    return roof, layer, {n: v[0] * 1e3 for n, v in kern.items()}, sha
 
-    # End-to-end through the C ABI with host buffers (pinned), copies timed.
+
+def force_flag(name):
+    from w4a16_compact_expert_gb300 import moe_w4a16 as M
+    return {"auto": 0, "gemv": M.FORCE_GEMV, "unfused": M.FORCE_GEMV | M.UNFUSED, "gemm": M.FORCE_GEMM}[name]
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    from w4a16_compact_expert_gb300 import build_ext, moe_w4a16
+    build_ext.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    T = tokens_of(args)
+    steps = args.steps or (4000 if T <= 64 else 100)
+    warm = max(3, args.warmup)
+    force = force_flag(args.force)
+    peaks = load_peaks()
+    wl = Workload(args, T, dev, local_rank)
+    avg_u = wl.unique_experts(force)
+    for m in wl.layers:
+        st, miss = m.get_status()
+        assert st == moe_w4a16.OK and miss == 0, (st, miss)
+    stream = torch.cuda.Stream(device=dev)
+    ms, clocks = time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks)
+    path, launches = wl.layers[0].last_path()
+    assert all(m.last_path() == (path, launches) for m in wl.layers)
+    value = wl.L * T * steps * world / (ms / 1e3)
+    stage_avg = stage_times(wl, force, stream)
+    layer_ms = ms / (steps * wl.L)
+    roof, layer, kern_us, sha = roofline(wl, path, layer_ms, stage_avg, avg_u, peaks)
     e2e_steps = max(10, min(200, steps // 10))
-    xh = [[xs[l][r].cpu().pin_memory() for r in range(ROTATE)] for l in range(LAYERS)]
-    oh = [torch.empty(T, H, dtype=torch.float16).pin_memory() for _ in range(LAYERS)]
-    for r in range(2):
-        for l, m in enumerate(layers):
-            m.forward_host(xh[l][r], rws[l], None, force, out_host=oh[l])
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        for l, m in enumerate(layers):
-            m.forward_host(xh[l][i % ROTATE], rws[l], None, force, out_host=oh[l])
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = LAYERS * T * e2e_steps * world / e2e_s
-
+    e2e = e2e_rate(wl, force, e2e_steps, world, local_rank)
+    s = wl.shape
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 weights x fp16 activations, fp32 accumulate", "data": "synthetic (seeded)",
         "config": workload_config(args, T) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                             "path": pname, "cuda_graph": True},
-        "roofline": {"bound": "tensor" if tensor else "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "peak_source": peak_src,
-                     "avg_launch_us": dom_ms * 1e3, "traffic": profiled_traffic(dom, T, sha)} | work,
-        "layer_roofline": {"algorithmic_bytes_per_layer": layer_bytes, "us_per_layer": layer_ms * 1e3,
-                           "achieved_gbs": layer_bytes / (layer_ms / 1e3) / 1e9,
-                           "hbm_frac": layer_bytes / (layer_ms / 1e3) / 1e9 / hbm,
-                           "achieved_tflops": layer_flops / (layer_ms / 1e3) / 1e12,
-                           "avg_unique_experts": avg_u},
-        "kernel_us": {n: v[0] * 1e3 for n, v in kern.items()},
+                                             "path": moe_w4a16.PATH_NAMES[path], "cuda_graph": True},
+        "roofline": roof, "layer_roofline": layer, "kernel_us": kern_us,
         "stage_event_us": [v * 1e3 for v in stage_avg],
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": LAYERS * T * H * 2,
-                "d2h_bytes_per_step": LAYERS * T * H * 2, "steps": e2e_steps},
-        "gpu_launches": steps * LAYERS * launches,
-        "launches_per_layer_forward": launches,
-        "clocks": clk.summary(peaks.get("sm_max_mhz")),
-        "kernel_src": sha,
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": wl.L * T * s.H * 2,
+                "d2h_bytes_per_step": wl.L * T * s.H * 2, "steps": e2e_steps},
+        "gpu_launches": steps * wl.L * launches, "launches_per_layer_forward": launches,
+        "clocks": clocks, "kernel_src": sha,
     }
-    for m in layers:
-        m.close()
+    wl.close()
     return res
+
+
+def stack_sweep(args, rank, world, local_rank):
+    """T sweep of the 16-layer stack with each kernel family forced; crossover T*."""
+    import torch
+    from w4a16_compact_expert_gb300 import build_ext, moe_w4a16
+    build_ext.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    rows = []
+    for T in SWEEP_T:
+        a = argparse.Namespace(**vars(args))
+        a.tokens = T
+        wl = Workload(a, T, dev, local_rank)
+        row = {"T": T}
+        for fam in ("gemv", "gemm"):
+            force = force_flag(fam)
+            steps = args.steps or max(5, min(400, 4096 // T))
+            ms, clocks = time_graphs(wl, force, steps, 3, stream, world, local_rank, peaks)
+            path, _ = wl.layers[0].last_path()
+            row[fam] = {"tokens_per_s_per_layer": T * steps * world / (ms / 1e3),
+                        "us_per_layer": ms * 1e3 / (steps * wl.L), "path": moe_w4a16.PATH_NAMES[path],
+                        "sm_mhz": clocks["sm_mhz"], "reasons": clocks["reasons"]}
+        for m in wl.layers:
+            st, miss = m.get_status()
+            assert st == moe_w4a16.OK and miss == 0, (st, miss)
+        wl.close()
+        del wl
+        torch.cuda.empty_cache()
+        rows.append(row)
+    cross = next((r["T"] for r in rows if r["gemm"]["us_per_layer"] < r["gemv"]["us_per_layer"]), None)
+    return {"metric": "per-layer tokens/s of the 16-layer OLMoE-shaped stack, decode kernels vs grouped GEMM",
+            "unit": UNIT, "n_gpus": world, "config": workload_config(args, 0) | {"sweep_T": SWEEP_T},
+            "rows": rows, "crossover_T": cross,
+            "crossover_note": "smallest swept T at which the grouped GEMM is faster than the decode kernels"}
 
 
 def main():
@@ -414,8 +586,7 @@ def main():
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                "data": "synthetic (seeded)", "config": workload_config(args, T),
                "cpu_baseline": {"value": leg["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{leg['steps']} float64-oracle forwards of one {args.workload} layer at "
-                                          f"T={T} (bounded by steps and 150 s)"},
+                                "sample": cpu_sample_text(args, leg) + " (bounded by steps and 150 s)"},
                "e2e": {"value": leg["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(res))
         return
@@ -423,15 +594,17 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    # CPU baseline first, in its own process, before this process touches the GPU.
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        leg = run_cpu_leg(args, seconds=args.cpu_seconds)
-        cpu = {"value": leg["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{leg['steps']} float64-oracle forwards of one OLMoE-shaped layer at T={T} in "
-                         f"{leg['seconds']:.1f} s, 1 thread"}
-    res = gpu_arm(args, rank, world, local_rank)
-    res["cpu_baseline"] = cpu
+    if args.sweep:
+        res = stack_sweep(args, rank, world, local_rank)
+    else:
+        # CPU baseline first, in its own process, before this process touches the GPU.
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            leg = run_cpu_leg(args, seconds=args.cpu_seconds)
+            cpu = {"value": leg["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": cpu_sample_text(args, leg)}
+        res = gpu_arm(args, rank, world, local_rank)
+        res["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
