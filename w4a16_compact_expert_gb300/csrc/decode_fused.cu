@@ -53,6 +53,7 @@ constexpr int kMaxT = 16;                      // tokens of the fused path (all 
 constexpr int kMaxP = kMaxT * 32;
 constexpr int kMaxSlots = 16;                  // ring entries
 constexpr int kMinSlots = 4;
+constexpr int kInFlight = 4;                   // ring entries in flight at once (bandwidth x latency per SM)
 constexpr int kMaxExperts = 256;               // readiness counters per handle
 constexpr uint32_t kSmemBudget = 226 * 1024;
 
@@ -76,8 +77,8 @@ __host__ __device__ inline FusedSmem fused_smem(const SlotLayout& lay, int H, in
   const uint32_t xa = ((uint32_t)T * (H + 8) * 2 + 127) / 128 * 128;
   const uint32_t ha = ((uint32_t)NG * hrows * (I + 8) * 2 + 127) / 128 * 128;
   const uint32_t red = (uint32_t)kCW * 2 * 16 * ntok * 4;
-  // per-chunk sums: x rows [T][H/64], per-group h rows [min(T, 8)][I/64]
-  const uint32_t sbb = ((uint32_t)(T * (H / 64) + NG * hrows * (I / 64)) * 4 + 127) / 128 * 128;
+  // per-chunk prefix sums: x rows [T][H/64 + 1], per-group h rows [min(T, 8)][I/64 + 1]
+  const uint32_t sbb = ((uint32_t)(T * (H / 64 + 1) + NG * hrows * (I / 64 + 1)) * 4 + 127) / 128 * 128;
   const int P = T * k;
   // logits [T][E] | ids, topw, sorted [P] | rnorm [T] | table, cnt, off [E + 1]
   // | active slot, start, count [E + 1] | chunk counts [ceil(P/32)][E] | misc
@@ -214,23 +215,15 @@ DEV_INLINE float warp_dot_part(const __half* xt, const __half* we, int k0, int k
   return warp_sum(acc);
 }
 
-// One 64-wide K chunk of a 16-row tile against NT n-tiles of 8 tokens.
+// MMA of one 64-wide K chunk (four 16x8x16 steps) of a 16-row tile against
+// NT n-tiles of 8 tokens, into c[nt] (which the caller zeroes per block).
 // The int4 nibbles enter the MMA as FP16 bit patterns with no arithmetic:
 //   row g     : 1024 + u          (u = q + 8 of row g)
 //   row g + 8 : 1024 + u + 16 u'  (u' = q + 8 of row g + 8, the row-g nibble
 //                                  of the same K left in place)
-// and the chunk's exact sum over K of q * b per row follows in FP32:
-//   row g     : c0 - 1032 S       row g + 8 : (c2 - c0 - 128 S) / 16
-// with S the chunk's sum of b for that token column; times the row's block
-// scale this accumulates into acc (sum_k q s b with q s exact, FP32).
+// block_epilogue() recovers the exact sum over K of q * b per row in FP32.
 template <int NT>
-DEV_INLINE void mma_chunk(float (&acc)[2][4], const uint4& q, float sg, float sg8, const uint4 (&bl)[NT],
-                          const uint4 (&bh)[NT], const float (&sb)[NT][2]) {
-  float c4[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) c4[nt][r] = 0.f;
+DEV_INLINE void mma_chunk(float (&c)[NT][4], const uint4& q, const uint4 (&bl)[NT], const uint4 (&bh)[NT]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t w = j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
@@ -242,70 +235,140 @@ DEV_INLINE void mma_chunk(float (&acc)[2][4], const uint4& q, float sg, float sg
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const uint4& bv = j < 2 ? bl[nt] : bh[nt];
-      mma_16816(c4[nt], a, (j & 1) ? bv.z : bv.x, (j & 1) ? bv.w : bv.y);
+      mma_16816(c[nt], a, (j & 1) ? bv.z : bv.x, (j & 1) ? bv.w : bv.y);
     }
   }
+}
+
+// For the chunks [k0, k1) of one 256-wide scale block: with c0..c3 the MMA
+// sums and S the sum of b over those chunks for the column,
+//   row g     : sum q b = c0 - 1032 S          (1024 + u = 1032 + q)
+//   row g + 8 : sum q b = (c2 - c0 - 128 S) / 16
+// times the row's block scale, accumulated in FP32 (q * s exact).
+// pre[nt][h]: prefix sums over chunks of the B column (2 cc + h of n-tile nt).
+template <int NT, int NC>
+DEV_INLINE void block_epilogue(float (&acc)[2][4], const float (&c)[NC][NT][4], float sg, float sg8,
+                               const float* const (&pre)[2][2], int k0, int k1) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    acc[nt][0] = fmaf(sg, fmaf(-1032.f, sb[nt][0], c4[nt][0]), acc[nt][0]);
-    acc[nt][1] = fmaf(sg, fmaf(-1032.f, sb[nt][1], c4[nt][1]), acc[nt][1]);
-    acc[nt][2] = fmaf(sg8, fmaf(-128.f, sb[nt][0], c4[nt][2] - c4[nt][0]), acc[nt][2]);
-    acc[nt][3] = fmaf(sg8, fmaf(-128.f, sb[nt][1], c4[nt][3] - c4[nt][1]), acc[nt][3]);
+    const float s0 = pre[nt][0][k1] - pre[nt][0][k0], s1 = pre[nt][1][k1] - pre[nt][1][k0];
+    float v0 = c[0][nt][0], v1 = c[0][nt][1], v2 = c[0][nt][2], v3 = c[0][nt][3];
+#pragma unroll
+    for (int i = 1; i < NC; ++i) {
+      v0 += c[i][nt][0];
+      v1 += c[i][nt][1];
+      v2 += c[i][nt][2];
+      v3 += c[i][nt][3];
+    }
+    acc[nt][0] = fmaf(sg, fmaf(-1032.f, s0, v0), acc[nt][0]);
+    acc[nt][1] = fmaf(sg, fmaf(-1032.f, s1, v1), acc[nt][1]);
+    acc[nt][2] = fmaf(sg8, fmaf(-128.f, s0, v2 - v0), acc[nt][2]);
+    acc[nt][3] = fmaf(sg8, fmaf(-128.f, s1, v3 - v1), acc[nt][3]);
   }
 }
 
-// acc[nt] += tile (16 x K) x B over the warp's K chunks kc0, kc0 + kstride,
-// ... < nkc.  brow[nt]: the lane's B row (token nt * 8 + lane / 4; any valid
-// row for columns past the tokens) in shared memory, K contiguous; sbc[nt]:
-// the per-chunk sums of the B rows of the lane's two output columns.
+// acc[nt] += tile (16 x K) x B over the warp's contiguous K chunks [c0, c1).
+// brow[nt]: the lane's B row (token nt * 8 + lane / 4; any valid row for
+// columns past the tokens) in shared memory, K contiguous; pre: see above.
+// Generic: any range (the block epilogue runs at block ends and at c1).
 template <int NT>
 DEV_INLINE void mma_fold(float (&acc)[2][4], const uint8_t* tile, uint32_t scale_bytes,
-                         const __half* const (&brow)[2], const float* const (&sbc)[2][2], int lane, int kc0,
-                         int kstride, int nkc) {
-  const int g = lane >> 2, c = lane & 3;
+                         const __half* const (&brow)[2], const float* const (&pre)[2][2], int lane, int c0, int c1) {
+  const int g = lane >> 2, cc = lane & 3;
   const uint8_t* qp = tile + scale_bytes + lane * 16;
   const __half* scp = reinterpret_cast<const __half*>(tile) + g;
-  constexpr int kB = 4;   // chunks whose operands are loaded ahead together
-  int kc = kc0;
-  for (; kc + (kB - 1) * kstride < nkc; kc += kB * kstride) {
-    uint4 q[kB], bl[kB][NT], bh[kB][NT];
-    float sg[kB], sg8[kB], sb[kB][NT][2];
+  int kc = c0;
+  while (kc < c1) {
+    const int bend = ((kc >> 2) + 1) * 4;
+    const int e = bend < c1 ? bend : c1;
+    float c[2][NT][4];   // two accumulator chains (even / odd chunks of the block)
 #pragma unroll
-    for (int i = 0; i < kB; ++i) {
-      const int k2 = kc + i * kstride;
-      q[i] = *reinterpret_cast<const uint4*>(qp + (size_t)k2 * 512);
-      sg[i] = __half2float(scp[(k2 >> 2) * 16]);
-      sg8[i] = __half2float(scp[(k2 >> 2) * 16 + 8]) * 0.0625f;
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        bl[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + c * 16);
-        bh[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + c * 16 + 8);
-        sb[i][nt][0] = sbc[nt][0][k2];
-        sb[i][nt][1] = sbc[nt][1][k2];
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) c[i][nt][r] = 0.f;
+    for (int k = kc; k < e; k += 2) {
+      const bool two = k + 1 < e;
+      uint4 q[2], bl[2][NT], bh[2][NT];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k2 = (i == 0 || two) ? k + i : k;   // a missing odd chunk reloads the even one, unused
+        q[i] = *reinterpret_cast<const uint4*>(qp + (size_t)k2 * 512);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          bl[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + cc * 16);
+          bh[i][nt] = *reinterpret_cast<const uint4*>(brow[nt] + k2 * 64 + cc * 16 + 8);
+        }
       }
+      mma_chunk<NT>(c[0], q[0], bl[0], bh[0]);
+      if (two) mma_chunk<NT>(c[1], q[1], bl[1], bh[1]);
     }
-#pragma unroll
-    for (int i = 0; i < kB; ++i) mma_chunk<NT>(acc, q[i], sg[i], sg8[i], bl[i], bh[i], sb[i]);
-  }
-  for (; kc < nkc; kc += kstride) {
-    uint4 bl[NT], bh[NT];
-    float sb[NT][2];
-    const uint4 q = *reinterpret_cast<const uint4*>(qp + (size_t)kc * 512);
     const float sg = __half2float(scp[(kc >> 2) * 16]);
     const float sg8 = __half2float(scp[(kc >> 2) * 16 + 8]) * 0.0625f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      bl[nt] = *reinterpret_cast<const uint4*>(brow[nt] + kc * 64 + c * 16);
-      bh[nt] = *reinterpret_cast<const uint4*>(brow[nt] + kc * 64 + c * 16 + 8);
-      sb[nt][0] = sbc[nt][0][kc];
-      sb[nt][1] = sbc[nt][1][kc];
-    }
-    mma_chunk<NT>(acc, q, sg, sg8, bl, bh, sb);
+    block_epilogue<NT, 2>(acc, c, sg, sg8, pre, kc, e);
+    kc = e;
   }
 }
 
-// Per-chunk sums of n FP16 rows [n][stride] over K (nk chunks of 64) ->
-// out[row * nk + chunk], by threads t0, t0 + nthr, ...
+// The same for a range of CPW chunks (a multiple of 4) starting on a block
+// boundary: fully unrolled, about 1.5x faster than the generic loop (the
+// compiler schedules the loads of all CPW chunks ahead of their MMAs).
+template <int NT, int CPW>
+DEV_INLINE void mma_fold_static(float (&acc)[2][4], const uint8_t* tile, uint32_t scale_bytes,
+                                const __half* const (&brow)[2], const float* const (&pre)[2][2], int lane,
+                                int c0) {
+  const int g = lane >> 2, cc = lane & 3;
+  const uint8_t* qp = tile + scale_bytes + lane * 16 + (size_t)c0 * 512;
+  const __half* scp = reinterpret_cast<const __half*>(tile) + g + (c0 >> 2) * 16;
+  const __half* bp[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) bp[nt] = brow[nt] + c0 * 64 + cc * 16;
+#pragma unroll
+  for (int bk = 0; bk < CPW / 4; ++bk) {
+    float c[4][NT][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) c[i][nt][r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = bk * 4 + i;
+      const uint4 q = *reinterpret_cast<const uint4*>(qp + ch * 512);
+      uint4 bl[NT], bh[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bl[nt] = *reinterpret_cast<const uint4*>(bp[nt] + ch * 64);
+        bh[nt] = *reinterpret_cast<const uint4*>(bp[nt] + ch * 64 + 8);
+      }
+      mma_chunk<NT>(c[i], q, bl, bh);
+    }
+    const float sg = __half2float(scp[bk * 16]);
+    const float sg8 = __half2float(scp[bk * 16 + 8]) * 0.0625f;
+    block_epilogue<NT, 4>(acc, c, sg, sg8, pre, c0 + bk * 4, c0 + bk * 4 + 4);
+  }
+}
+
+// Dispatch on the warp's chunk range.
+template <int NT>
+DEV_INLINE void mma_range(float (&acc)[2][4], const uint8_t* tile, uint32_t scale_bytes,
+                          const __half* const (&brow)[2], const float* const (&pre)[2][2], int lane, int c0, int c1) {
+  // one token tile over whole scale blocks (the OLMoE- and Qwen-shaped gate/up
+  // and the OLMoE down at 4 warps per group): the unrolled form block by
+  // block (a block's operands fit the 128 registers a thread has here); the
+  // loop otherwise
+  if (NT == 1 && (c0 & 3) == 0 && ((c1 - c0) & 3) == 0) {
+    for (int b0 = c0; b0 < c1; b0 += 4) mma_fold_static<NT, 4>(acc, tile, scale_bytes, brow, pre, lane, b0);
+  } else {
+    mma_fold<NT>(acc, tile, scale_bytes, brow, pre, lane, c0, c1);
+  }
+}
+
+// Prefix sums over K chunks of n FP16 rows [n][stride] (nk chunks of 64):
+// out[row * (nk + 1) + j] = sum of the row's values in chunks < j.  Two steps
+// separated by the caller's barrier: chunk_sums() then chunk_prefix().
 DEV_INLINE void chunk_sums(float* out, const __half* rows, int stride, int n, int nk, int t0, int nthr) {
   for (int i = t0; i < n * nk; i += nthr) {
     const int r = i / nk, kc = i - r * nk;
@@ -321,7 +384,19 @@ DEV_INLINE void chunk_sums(float* out, const __half* rows, int stride, int n, in
         s += f.x + f.y;
       }
     }
-    out[i] = s;
+    out[r * (nk + 1) + kc + 1] = s;
+  }
+}
+
+DEV_INLINE void chunk_prefix(float* out, int n, int nk, int t0, int nthr) {
+  for (int r = t0; r < n; r += nthr) {
+    float* o = out + r * (nk + 1);
+    float s = 0.f;
+    o[0] = 0.f;
+    for (int j = 1; j <= nk; ++j) {
+      s += o[j];
+      o[j] = s;
+    }
   }
 }
 
@@ -364,8 +439,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   __half* xcache = reinterpret_cast<__half*>(sm + L.off_x);
   __half* hstage = reinterpret_cast<__half*>(sm + L.off_h);
   float* red = reinterpret_cast<float*>(sm + L.off_red);
-  float* sb_x = reinterpret_cast<float*>(sm + L.off_sb);        // [T][H/64]
-  float* sb_h = sb_x + T * (H / 64);                             // per group [min(T, 8)][I/64]
+  float* sb_x = reinterpret_cast<float*>(sm + L.off_sb);        // [T][H/64 + 1] prefix sums
+  float* sb_h = sb_x + T * (H / 64 + 1);                         // per group [min(T, 8)][I/64 + 1]
   float* lg = reinterpret_cast<float*>(sm + L.off_route);   // [T][E]
   int* r_ids = reinterpret_cast<int*>(lg + T * E);
   float* r_w = reinterpret_cast<float*>(r_ids + P);
@@ -430,30 +505,106 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   }
 
   // ------------------------------------------ routing in shared memory
-  for (int i = tid; i < T * E; i += blockDim.x) lg[i] = __ldcg(&c.logit_part[i]) + __ldcg(&c.logit_part[T * E + i]);
-  if (c.flags & 2u)
-    for (int t = tid; t < T; t += blockDim.x)
-      r_rnorm[t] = prenorm_scale(__ldcg(&c.ss_part[t]) + __ldcg(&c.ss_part[T + t]), H);
-  for (int e = tid; e < ((P + 31) / 32) * E; e += blockDim.x) r_chunk[e] = 0;
-  __syncthreads();
+  const int nchunk = (P + 31) / 32;
+  for (int e = tid; e < nchunk * E; e += blockDim.x) r_chunk[e] = 0;
   {
     FwdCtx cl = c;   // top-k results go to shared memory
     cl.ids = r_ids;
     cl.topw = r_w;
-    for (int t = warp; t < T; t += kNW)
-      topk_token(cl, t, lg + t * E, (c.flags & 2u) ? r_rnorm[t] : 1.f, nullptr);
+    for (int t = warp; t < T; t += kNW) {
+      // the token's logits: its two K-half partial sums, straight from global memory
+      for (int e = lane; e < E; e += 32)
+        lg[t * E + e] = __ldcg(&c.logit_part[t * E + e]) + __ldcg(&c.logit_part[T * E + t * E + e]);
+      float r = 1.f;
+      if (c.flags & 2u) {
+        r = prenorm_scale(__ldcg(&c.ss_part[t]) + __ldcg(&c.ss_part[T + t]), H);
+        if (lane == 0) r_rnorm[t] = r;
+      }
+      __syncwarp();
+      topk_token(cl, t, lg + t * E, r, nullptr);
+    }
   }
-  __syncthreads();
-  // counts per 32-pair chunk: __match_any_sync groups equal ids (no atomics)
-  const int nchunk = (P + 31) / 32;
-  for (int ch = warp; ch < nchunk; ch += kNW) {
+  __syncthreads();   // top-k ids and weights of every token
+  const int tpe1 = I / 16, tpe2 = H / kDownRows;
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    // The active experts (routed and resident), ascending, straight from the
+    // ids: a warp-wide union bitmask, so the weight stream starts while the
+    // other warps count, scan and scatter.
+    int U = 0;
+    for (int w0 = 0; w0 < E; w0 += 32) {
+      unsigned bits = 0;
+      for (int p = lane; p < P; p += 32) {
+        const int e = r_ids[p];
+        if (e >= w0 && e < w0 + 32) bits |= 1u << (e - w0);
+      }
+      bits = __reduce_or_sync(kFull, bits);
+      const int e = w0 + lane;
+      const bool act = e < E && ((bits >> lane) & 1u) && r_table[e] >= 0;
+      const unsigned am = __ballot_sync(kFull, act);
+      if (act) r_aslot[U + __popc(am & ((1u << lane) - 1u))] = r_table[e];
+      U += __popc(am);
+    }
+    __syncwarp();
+    const int n1 = U * tpe1, n2 = U * tpe2;
+    const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
+    const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
+    // entries: 2j (gate tile) and 2j + 1 (up tile) of gate/up item j < m1,
+    // then 2 m1 + j (the 2 row tiles of down item j < m2); entry e -> slot e % NS
+    if (lane == 0) {
+      const int ne = 2 * m1 + m2;
+      int issued = 0;
+      for (int e = 0; e < ne; ++e) {
+        const int s = e % NS;
+        if (!wait_phase(&empty[s], (uint32_t)((e / NS) & 1) ^ 1u, &s_abort, c.status)) break;
+        // at most kInFlight entries on their way: copies issued together share
+        // the bandwidth and land together, so a bounded window lets the first
+        // entries land (and compute start) early.  Entry e - kInFlight's slot
+        // cannot hold a newer entry yet, so its parity is unambiguous.
+        if (e >= kInFlight) {
+          const int ep = e - kInFlight;
+          if (!wait_phase(&full[ep % NS], (uint32_t)((ep / NS) & 1), &s_abort, c.status)) break;
+        }
+        s_seq[s] = e;
+        uint8_t* dst = sm + (size_t)s * L.slot_bytes;
+        if (e < 2 * m1) {
+          const int it = a1 + (e >> 1), u = it / tpe1, rt = it % tpe1;
+          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
+          const MatLayout& M = (e & 1) ? c.lay.up : c.lay.gate;
+          mbar_expect_tx(&full[s], M.tile_bytes);
+          bulk_g2s(dst, tile_ptr(base, M, rt), M.tile_bytes, &full[s]);
+        } else {
+          const int it = a2 + (e - 2 * m1), u = it / tpe2, hb = it % tpe2;
+          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
+          const uint32_t bytes = 2 * c.lay.down.tile_bytes;   // the 2 row tiles of a block are contiguous
+          mbar_expect_tx(&full[s], bytes);
+          bulk_g2s(dst, tile_ptr(base, c.lay.down, 2 * hb), bytes, &full[s]);
+        }
+        issued = e + 1;
+      }
+      // copies in flight land before the CTA (and its shared memory) ends:
+      // only the last entry issued into a slot can still be pending
+      for (int s = 0; s < NS && s < issued; ++s) {
+        const int last = s + (issued - 1 - s) / NS * NS;
+        mbar_wait_bounded(&full[s], (uint32_t)((last / NS) & 1), c.status);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------- counts, scan, active groups
+  // (every warp but the producer: named barrier 6, 13 warps)
+  const int wr = warp < kCW ? warp : kCW;   // the signaller takes the producer's turn
+  for (int ch = wr; ch < nchunk; ch += kNW - 1) {
+    // counts per 32-pair chunk: __match_any_sync groups equal ids (no atomics)
     const int p = ch * 32 + lane;
     const int e = p < P ? r_ids[p] : -1 - lane;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (p < P && __popc(peers & ((1u << lane) - 1u)) == 0) r_chunk[ch * E + e] = __popc(peers);
   }
-  __syncthreads();
-  if (warp == 0) {   // counts, exclusive scan, active list (ascending experts)
+  named_sync(6, (kNW - 1) * 32);
+  if (warp == 0) {   // counts, exclusive scan, active groups (ascending experts)
     const int per = (E + 31) / 32;
     int local[kMaxEPL];
     int s = 0;
@@ -495,7 +646,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       const unsigned am = __ballot_sync(kFull, act);
       const int pos = n + __popc(am & ((1u << lane) - 1u));
       if (act) {
-        r_aslot[pos] = slot;
         r_astart[pos] = r_off[e];
         r_acount[pos] = ce;
       }
@@ -503,49 +653,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     }
     if (lane == 0) r_misc[0] = n;
   }
-  __syncthreads();
+  named_sync(6, (kNW - 1) * 32);
   const int U = r_misc[0];
-  const int tpe1 = I / 16, tpe2 = H / kDownRows;
   const int n1 = U * tpe1, n2 = U * tpe2;
   const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
   const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
-
-  if (warp == kCW) {
-    // ------------------------------------------------------------ producer
-    // entries: 2j (gate tile) and 2j + 1 (up tile) of gate/up item j < m1,
-    // then 2 m1 + j (the 2 row tiles of down item j < m2); entry e -> slot e % NS
-    if (lane == 0) {
-      const int ne = 2 * m1 + m2;
-      int issued = 0;
-      for (int e = 0; e < ne; ++e) {
-        const int s = e % NS;
-        if (!wait_phase(&empty[s], (uint32_t)((e / NS) & 1) ^ 1u, &s_abort, c.status)) break;
-        s_seq[s] = e;
-        uint8_t* dst = sm + (size_t)s * L.slot_bytes;
-        if (e < 2 * m1) {
-          const int it = a1 + (e >> 1), u = it / tpe1, rt = it % tpe1;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const MatLayout& M = (e & 1) ? c.lay.up : c.lay.gate;
-          mbar_expect_tx(&full[s], M.tile_bytes);
-          bulk_g2s(dst, tile_ptr(base, M, rt), M.tile_bytes, &full[s]);
-        } else {
-          const int it = a2 + (e - 2 * m1), u = it / tpe2, hb = it % tpe2;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const uint32_t bytes = 2 * c.lay.down.tile_bytes;   // the 2 row tiles of a block are contiguous
-          mbar_expect_tx(&full[s], bytes);
-          bulk_g2s(dst, tile_ptr(base, c.lay.down, 2 * hb), bytes, &full[s]);
-        }
-        issued = e + 1;
-      }
-      // copies in flight land before the CTA (and its shared memory) ends:
-      // only the last entry issued into a slot can still be pending
-      for (int s = 0; s < NS && s < issued; ++s) {
-        const int last = s + (issued - 1 - s) / NS * NS;
-        mbar_wait_bounded(&full[s], (uint32_t)((last / NS) & 1), c.status);
-      }
-    }
-    return;
-  }
 
   if (warp == kCW + 1) {
     // ----------------------------------------------------------- signaller
@@ -620,6 +732,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   named_sync(1, kCW * 32);
   chunk_sums(sb_x, xcache, H + 8, T, H / 64, tid, kCW * 32);   // x rows landed (xbar) before the barrier
   named_sync(1, kCW * 32);
+  chunk_prefix(sb_x, T, H / 64, tid, kCW * 32);
+  named_sync(1, kCW * 32);
   if (U == 0) {   // every routed expert is absent: out = residual or 0
     for (int i = b * kCW * 32 + tid; i < T * H; i += G * kCW * 32)
       c.out[i] = (c.flags & 1u) ? c.x[i] : __float2half_rn(0.f);
@@ -645,7 +759,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       const int ntl = cnt > 8 ? 2 : 1;
       const int tok0 = r_sorted[start] / k;
       const __half* brow[2];
-      const float* sbc[2][2];
+      const float* pre[2][2];
+      const int nkh = H / 64;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int ti = nt * 8 + g;   // the lane's B row; rows past cnt feed discarded columns
@@ -653,9 +768,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int tc = nt * 8 + 2 * cc + h;   // the lane's output columns
-          sbc[nt][h] = sb_x + (size_t)(tc < cnt ? r_sorted[start + tc] / k : tok0) * (H / 64);
+          pre[nt][h] = sb_x + (size_t)(tc < cnt ? r_sorted[start + tc] / k : tok0) * (nkh + 1);
         }
       }
+      const int kc0 = wq * nkh / GW, kc1 = (wq + 1) * nkh / GW;   // the warp's K chunks
       float acc[2][2][4];
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
@@ -667,9 +783,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
         warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
         const uint8_t* tile = sm + (size_t)s * L.slot_bytes;
         if (ntl == 1)
-          mma_fold<1>(acc[mat], tile, c.lay.gate.scale_bytes, brow, sbc, lane, wq, GW, H / 64);
+          mma_range<1>(acc[mat], tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
         else
-          mma_fold<2>(acc[mat], tile, c.lay.gate.scale_bytes, brow, sbc, lane, wq, GW, H / 64);
+          mma_range<2>(acc[mat], tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with the entry
       }
@@ -718,7 +834,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
       for (int p0 = 0; p0 < cnt; p0 += kTok) {
         const int np = min(kTok, cnt - p0);
-        float* sbg = sb_h + (size_t)q * (T < kTok ? T : kTok) * (I / 64);   // this group's h chunk sums
+        float* sbg = sb_h + (size_t)q * (T < kTok ? T : kTok) * (I / 64 + 1);   // this group's h prefix sums
         if (u != staged_u || p0 != staged_p0) {
           named_sync(gbar, GW * 32);   // readiness seen by the leader; the group is done with hs
           const int vpr = I / 8;       // the np rows are consecutive in hbuf
@@ -728,16 +844,19 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
           cp_async_wait_all();
           named_sync(gbar, GW * 32);
           chunk_sums(sbg, hs, I + 8, np, I / 64, gtid, GW * 32);
+          named_sync(gbar, GW * 32);
+          chunk_prefix(sbg, np, I / 64, gtid, GW * 32);
           staged_u = u;
           staged_p0 = p0;
         }
         named_sync(gbar, GW * 32);   // staged rows and sums visible; previous pass done with rg
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const __half* const brow[2] = {hs + (size_t)(g < np ? g : 0) * (I + 8), hs};
-        const float* const sbc[2][2] = {{sbg + (size_t)(2 * cc < np ? 2 * cc : 0) * (I / 64),
-                                         sbg + (size_t)(2 * cc + 1 < np ? 2 * cc + 1 : 0) * (I / 64)},
+        const int nki = I / 64, parts = GW / 2;
+        const float* const pre[2][2] = {{sbg + (size_t)(2 * cc < np ? 2 * cc : 0) * (nki + 1),
+                                         sbg + (size_t)(2 * cc + 1 < np ? 2 * cc + 1 : 0) * (nki + 1)},
                                         {sbg, sbg}};
-        mma_fold<1>(acc, tile, c.lay.down.scale_bytes, brow, sbc, lane, ks, GW / 2, I / 64);
+        mma_range<1>(acc, tile, c.lay.down.scale_bytes, brow, pre, lane, ks * nki / parts, (ks + 1) * nki / parts);
         float* rw = rg + wq * 16 * kTok;
         rw[g * kTok + 2 * cc] = acc[0][0];
         rw[g * kTok + 2 * cc + 1] = acc[0][1];
