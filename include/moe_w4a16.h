@@ -245,6 +245,124 @@ enum {
 };
 MOE_W4A16_API int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches);
 
+
+/* ======================================================================
+ * Expert cache: the partial-residency miss path.
+ *
+ * Follows the lifecycle of the pages' resident-qpacked-cache-v1 contract
+ * ("Horizon RunMap - architecture", section "Immutable authority and miss
+ * lifecycle"; "Immutable cache — the scope of ADR 0009"):
+ *   - the complete set of E experts stays in caller-owned host memory (the
+ *     immutable backing, canonical qpacked layout as for pack_experts) for
+ *     the cache's lifetime; it is never written;
+ *   - a miss reserves a bounded pinned staging entry and an unpublished
+ *     spare slot row; transport is backing -> pinned staging -> device
+ *     (repacked into the spare row); a staging entry is reused only after
+ *     its transfer-completion event has retired;
+ *   - once every miss of the routed group has been transferred, one new
+ *     complete generation of the expert->slot table is published
+ *     atomically: forwards enqueued on this handle afterwards read it,
+ *     forwards enqueued before keep reading the previous one;
+ *   - a consumer holds a lease on the generation it read; the row of an
+ *     evicted expert, and an old generation's table, are reused only after
+ *     every lease on an older generation has retired (its release event
+ *     completed);
+ *   - eviction discards the device copy (least recently used resident
+ *     expert outside the group, ties to the lower expert id); nothing is
+ *     ever copied device -> host (d2h_bytes stays 0);
+ *   - misses are serialised (one transaction at a time per cache);
+ *   - capacity is fixed at create, which rejects insufficient staging or
+ *     spare rows;
+ *   - a failure before publication leaves the previous generation
+ *     authoritative (the transaction's rows return to the spares); a
+ *     failure during or after publication faults the cache: every later
+ *     call returns MOE_W4A16_ERR_CUDA.
+ * While a cache is attached to a handle it owns the handle's slot rows and
+ * table: pack_experts and set_slot_table on the handle fail, and the handle
+ * must outlive the cache.  Forwards must run between acquire and release of
+ * a lease for the reuse guarantees to hold.
+ * ==================================================================== */
+typedef struct moe_w4a16_cache moe_w4a16_cache;
+
+typedef struct {
+  int32_t staging_experts; /* experts the pinned staging arena holds (>= 1) */
+  int32_t spare_slots;     /* slot rows kept out of the published table (>= max_group) */
+  int32_t max_group;       /* the most distinct experts one acquire may name (1..E) */
+} moe_w4a16_cache_config;
+
+typedef struct {
+  uint64_t generation;    /* published generation (1 after create) */
+  uint64_t transactions;  /* acquires that published a new generation */
+  uint64_t hits;          /* experts named by acquires that were resident */
+  uint64_t misses;        /* experts named by acquires that were transferred */
+  uint64_t evictions;     /* resident experts discarded */
+  uint64_t h2d_bytes;     /* expert bytes copied host -> device (canonical qpacked) */
+  uint64_t d2h_bytes;     /* expert bytes copied device -> host: always 0 */
+  uint64_t lease_waits;   /* times a transaction waited for older leases to retire */
+  int32_t resident;       /* experts in the published generation */
+  int32_t free_spares;    /* spare rows reusable now */
+  int32_t retiring;       /* rows waiting for older leases to retire */
+  int32_t active_leases;  /* leases not yet retired */
+  int32_t faulted;        /* 1 once a failure after publication began */
+} moe_w4a16_cache_stats;
+
+/* Creates a cache over handle h (its slot pool: num_slots rows) with the
+ * immutable host backing of all num_experts experts (six canonical arrays
+ * as in pack_experts, leading axis = expert id; host memory, caller-owned,
+ * unchanged until destroy) and places initial[0..n_initial) canonically in
+ * slots 0..n_initial-1 (generation 1).  Admission (ERR_INVALID_ARG):
+ * 1 <= max_group <= E, spare_slots >= max_group, staging_experts >= 1,
+ * n_initial + spare_slots <= num_slots, distinct valid initial ids.
+ * ERR_OOM when the staging arena cannot be allocated.  Synchronous. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_create(moe_w4a16_handle* h, const moe_w4a16_cache_config* cfg,
+                                                      const uint8_t* gate_q, const uint16_t* gate_s,
+                                                      const uint8_t* up_q, const uint16_t* up_s,
+                                                      const uint8_t* down_q, const uint16_t* down_s,
+                                                      const int32_t* initial, int32_t n_initial,
+                                                      moe_w4a16_cache** out);
+
+/* Waits for every outstanding lease and transfer, detaches and frees. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_destroy(moe_w4a16_cache* c);
+
+/* Makes the distinct experts ids[0..n) (n <= max_group) resident and hands
+ * out a lease on the generation that holds them.  All hits: no new
+ * generation.  Misses: transfers on `stream`, then publishes a new
+ * generation (the table copy is ordered on `stream` after the transfers).
+ * May wait on the host for older leases to retire when no spare row is
+ * reusable yet.  Errors: ERR_INVALID_ARG (bad ids, n > max_group),
+ * ERR_CUDA (transport failed before publication: old generation kept; or
+ * cache faulted), ERR_TIMEOUT (simulation: a needed lease never retires). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_acquire(moe_w4a16_cache* c, const int32_t* ids, int32_t n,
+                                                       moe_w4a16_stream_t stream, uint64_t* lease);
+
+/* Ends a lease once the work enqueued so far on `stream` completes (an
+ * event is recorded; the lease retires when it has completed). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_release(moe_w4a16_cache* c, uint64_t lease,
+                                                       moe_w4a16_stream_t stream);
+
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_get_stats(moe_w4a16_cache* c, moe_w4a16_cache_stats* out);
+
+/* Slot of `expert` in the published generation, -1 if not resident (or bad
+ * arguments). */
+MOE_W4A16_API int32_t moe_w4a16_cache_slot_of(const moe_w4a16_cache* c, int32_t expert);
+
+MOE_W4A16_API const char* moe_w4a16_cache_last_error(const moe_w4a16_cache* c);
+
+/* Host-only simulation: the same cache logic with a transport that moves
+ * no bytes and touches no GPU (no handle), for testing the lifecycle
+ * without a device.  Lease release events complete only when
+ * moe_w4a16_cache_sim_complete names them; a transaction that would have to
+ * wait for one returns ERR_TIMEOUT before publication.
+ * moe_w4a16_cache_sim_fail(c, 1) makes the next transaction's transport
+ * fail (before publication), (c, 2) its publication fail. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_create_sim(int32_t num_experts, int32_t num_slots,
+                                                          uint64_t expert_bytes,
+                                                          const moe_w4a16_cache_config* cfg,
+                                                          const int32_t* initial, int32_t n_initial,
+                                                          moe_w4a16_cache** out);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_sim_complete(moe_w4a16_cache* c, uint64_t lease);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_cache_sim_fail(moe_w4a16_cache* c, int32_t where);
+
 #ifdef __cplusplus
 }
 #endif

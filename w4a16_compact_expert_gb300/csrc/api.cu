@@ -16,45 +16,7 @@
 
 #include "moe_w4a16.h"
 #include "internal.h"
-
-struct moe_w4a16_handle {
-  moe_w4a16_config cfg{};
-  SlotLayout lay{};
-  int num_sms = 0;
-  int ksplit_fused = 1;
-  int max_smem = 0;                  // opt-in shared memory per block
-  int32_t gemv_max_tokens = 0;
-  int32_t last_path = 0;             // MOE_W4A16_PATH_* of the last forward
-  int32_t last_launches = 0;
-  uint8_t* pool = nullptr;
-  std::vector<uint8_t> packed;      // per slot: 1 once packed
-  std::vector<int32_t> h_table;
-  bool table_set = false;
-  int32_t* d_table = nullptr;
-  // workspaces
-  float* logit_part = nullptr;
-  float* ss_part = nullptr;
-  float* rnorm = nullptr;
-  int32_t* ids = nullptr;
-  float* topw = nullptr;
-  int32_t* offsets = nullptr;
-  int32_t* sorted = nullptr;
-  int32_t* p2r = nullptr;
-  int32_t* act = nullptr;            // 5 arrays of E (+1) ints, see fill_ctx
-  __half* xp = nullptr;
-  __half* hbuf = nullptr;
-  float* ybuf = nullptr;
-  unsigned* counters = nullptr;      // counter_words(H): grid barrier, arrival and readiness counters
-  DevStatus* status = nullptr;
-  uint8_t* stage = nullptr;          // pack staging for host sources
-  size_t stage_bytes = 0;
-  __half* x_dev = nullptr;           // forward_host staging
-  __half* out_dev = nullptr;
-  StageEvents events{};
-  PoolMaps maps{};
-  std::vector<void*> allocs;
-  std::string err;
-};
+#include "handle.h"
 
 namespace {
 
@@ -232,6 +194,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   if (e == cudaSuccess) e = cudaMemset(h->counters, 0, counter_words(H) * sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(h->d_table, 0xff, E * sizeof(int32_t));
+  h->cur_table = h->d_table;
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) h->maps = make_pool_maps(h->pool, h->lay, c.num_slots);
   if (e != cudaSuccess) {
@@ -248,6 +211,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
 
 moe_w4a16_status moe_w4a16_destroy(moe_w4a16_handle* h) {
   if (!h) return MOE_W4A16_OK;
+  if (h->cache) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "destroy the expert cache attached to this handle first");
   {
     DeviceGuard dg(h->cfg.device);
     cudaDeviceSynchronize();
@@ -286,6 +250,7 @@ moe_w4a16_status moe_w4a16_pack_experts(moe_w4a16_handle* h, int32_t slot0, int3
                                         const uint16_t* gate_s, const uint8_t* up_q, const uint16_t* up_s,
                                         const uint8_t* down_q, const uint16_t* down_s, moe_w4a16_stream_t stream) {
   if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  if (h->cache) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "an expert cache owns the slot rows of this handle");
   if (n < 0 || slot0 < 0 || (int64_t)slot0 + n > h->cfg.num_slots)
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "slot range [slot0, slot0+n) outside the pool");
   if (n == 0) return MOE_W4A16_OK;
@@ -331,6 +296,7 @@ moe_w4a16_status moe_w4a16_set_slot_table(moe_w4a16_handle* h, const int32_t* ex
                                           moe_w4a16_stream_t stream) {
   if (!h) return MOE_W4A16_ERR_INVALID_ARG;
   if (!expert_to_slot) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "expert_to_slot is NULL");
+  if (h->cache) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "an expert cache owns the slot table of this handle");
   const int E = h->cfg.num_experts, S = h->cfg.num_slots;
   std::vector<uint8_t> used(S, 0);
   for (int e = 0; e < E; ++e) {
@@ -348,6 +314,7 @@ moe_w4a16_status moe_w4a16_set_slot_table(moe_w4a16_handle* h, const int32_t* ex
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "set_slot_table");
   h->table_set = true;
+  h->cur_table = h->d_table;
   return MOE_W4A16_OK;
 }
 
@@ -360,7 +327,7 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.pool = h->pool;
   c.slot_bytes = h->lay.bytes;
   c.lay = h->lay;
-  c.table = h->d_table;
+  c.table = h->cur_table;
   c.logit_part = h->logit_part;
   c.ss_part = h->ss_part;
   c.rnorm = h->rnorm;

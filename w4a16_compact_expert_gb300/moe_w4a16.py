@@ -23,7 +23,11 @@ RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED = 1, 2, 4, 8, 16
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
             "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
             "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens",
-            "moe_w4a16_set_stage_events", "moe_w4a16_last_path"]
+            "moe_w4a16_set_stage_events", "moe_w4a16_last_path", "moe_w4a16_route_noalloc",
+            "moe_w4a16_cache_create", "moe_w4a16_cache_destroy", "moe_w4a16_cache_acquire",
+            "moe_w4a16_cache_release", "moe_w4a16_cache_get_stats", "moe_w4a16_cache_slot_of",
+            "moe_w4a16_cache_last_error", "moe_w4a16_cache_create_sim", "moe_w4a16_cache_sim_complete",
+            "moe_w4a16_cache_sim_fail"]
 PATH_NONE, PATH_DECODE_FUSED, PATH_DECODE, PATH_GEMM = 0, 1, 2, 3
 PATH_NAMES = {PATH_NONE: "none", PATH_DECODE_FUSED: "decode_fused", PATH_DECODE: "decode", PATH_GEMM: "gemm"}
 
@@ -32,6 +36,21 @@ class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("device", ctypes.c_int32)]
+
+
+class CacheConfig(ctypes.Structure):
+    _fields_ = [("staging_experts", ctypes.c_int32), ("spare_slots", ctypes.c_int32), ("max_group", ctypes.c_int32)]
+
+
+class CacheStats(ctypes.Structure):
+    _fields_ = [("generation", ctypes.c_uint64), ("transactions", ctypes.c_uint64), ("hits", ctypes.c_uint64),
+                ("misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64), ("h2d_bytes", ctypes.c_uint64),
+                ("d2h_bytes", ctypes.c_uint64), ("lease_waits", ctypes.c_uint64), ("resident", ctypes.c_int32),
+                ("free_spares", ctypes.c_int32), ("retiring", ctypes.c_int32), ("active_leases", ctypes.c_int32),
+                ("faulted", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class MoEError(RuntimeError):
@@ -69,6 +88,21 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_set_stage_events.argtypes = [vp, vp]
     lib.moe_w4a16_last_path.argtypes = [vp, ctypes.POINTER(i32)]
     lib.moe_w4a16_last_path.restype = i32
+    u64, u64p = ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)
+    lib.moe_w4a16_cache_create.argtypes = [vp, ctypes.POINTER(CacheConfig), vp, vp, vp, vp, vp, vp, vp, i32,
+                                           ctypes.POINTER(vp)]
+    lib.moe_w4a16_cache_create_sim.argtypes = [i32, i32, u64, ctypes.POINTER(CacheConfig), vp, i32,
+                                               ctypes.POINTER(vp)]
+    lib.moe_w4a16_cache_destroy.argtypes = [vp]
+    lib.moe_w4a16_cache_acquire.argtypes = [vp, vp, i32, vp, u64p]
+    lib.moe_w4a16_cache_release.argtypes = [vp, u64, vp]
+    lib.moe_w4a16_cache_get_stats.argtypes = [vp, ctypes.POINTER(CacheStats)]
+    lib.moe_w4a16_cache_slot_of.argtypes = [vp, i32]
+    lib.moe_w4a16_cache_slot_of.restype = i32
+    lib.moe_w4a16_cache_last_error.argtypes = [vp]
+    lib.moe_w4a16_cache_last_error.restype = ctypes.c_char_p
+    lib.moe_w4a16_cache_sim_complete.argtypes = [vp, u64]
+    lib.moe_w4a16_cache_sim_fail.argtypes = [vp, i32]
     _lib = lib
     return lib
 
@@ -199,3 +233,86 @@ class MoELayer:
         miss = ctypes.c_int64(0)
         st = self.lib.moe_w4a16_get_status(self.h, ctypes.byref(miss))
         return st, miss.value
+
+
+class ExpertCache:
+    """The partial-residency miss path (moe_w4a16_cache_*): an immutable host
+    backing of all experts, bounded pinned staging, spare slot rows,
+    generation publication, leases and LRU discard eviction.
+
+    ExpertCache(layer, backing, staging_experts, spare_slots, max_group, initial)
+    attaches to a MoELayer; ExpertCache.sim(num_experts, num_slots, ...) is the
+    host-only simulation (no GPU)."""
+
+    def __init__(self, layer=None, backing=None, staging_experts=1, spare_slots=1, max_group=1, initial=(),
+                 _sim=None):
+        self.lib = load_library()
+        self.cfg = CacheConfig(staging_experts, spare_slots, max_group)
+        init = np.ascontiguousarray(np.asarray(list(initial), dtype=np.int32))
+        h = ctypes.c_void_p()
+        if _sim is not None:
+            ne, ns, eb = _sim
+            st = self.lib.moe_w4a16_cache_create_sim(ne, ns, eb, ctypes.byref(self.cfg),
+                                                     init.ctypes.data if init.size else None, int(init.size),
+                                                     ctypes.byref(h))
+            self._keep = None
+        else:
+            arrays = [np.ascontiguousarray(a) for a in backing]
+            self._keep = arrays   # the immutable backing must outlive the cache
+            st = self.lib.moe_w4a16_cache_create(layer.h, ctypes.byref(self.cfg),
+                                                 *[a.ctypes.data for a in arrays],
+                                                 init.ctypes.data if init.size else None, int(init.size),
+                                                 ctypes.byref(h))
+        if st != OK:
+            raise MoEError(st, self.lib.moe_w4a16_last_error(None).decode())
+        self.c = h
+        self.layer = layer
+        self.is_sim = _sim is not None
+
+    def _st(self, stream):
+        return None if self.is_sim else _stream(stream)
+
+    @classmethod
+    def sim(cls, num_experts, num_slots, expert_bytes=1000, staging_experts=1, spare_slots=1, max_group=1,
+            initial=()):
+        return cls(None, None, staging_experts, spare_slots, max_group, initial,
+                   _sim=(num_experts, num_slots, expert_bytes))
+
+    def _check(self, st):
+        if st != OK:
+            raise MoEError(st, self.lib.moe_w4a16_cache_last_error(self.c).decode())
+
+    def acquire(self, ids, stream=None) -> int:
+        a = np.ascontiguousarray(np.asarray(list(ids), dtype=np.int32))
+        lease = ctypes.c_uint64(0)
+        self._check(self.lib.moe_w4a16_cache_acquire(self.c, a.ctypes.data if a.size else None, int(a.size),
+                                                     self._st(stream), ctypes.byref(lease)))
+        return lease.value
+
+    def release(self, lease: int, stream=None):
+        self._check(self.lib.moe_w4a16_cache_release(self.c, ctypes.c_uint64(lease), self._st(stream)))
+
+    def stats(self) -> dict:
+        s = CacheStats()
+        self._check(self.lib.moe_w4a16_cache_get_stats(self.c, ctypes.byref(s)))
+        return s.as_dict()
+
+    def slot_of(self, expert: int) -> int:
+        return self.lib.moe_w4a16_cache_slot_of(self.c, int(expert))
+
+    def sim_complete(self, lease: int):
+        self._check(self.lib.moe_w4a16_cache_sim_complete(self.c, ctypes.c_uint64(lease)))
+
+    def sim_fail(self, where: int):
+        self._check(self.lib.moe_w4a16_cache_sim_fail(self.c, int(where)))
+
+    def close(self):
+        if self.c:
+            self._check(self.lib.moe_w4a16_cache_destroy(self.c))
+            self.c = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
