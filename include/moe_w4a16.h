@@ -246,6 +246,18 @@ enum {
 MOE_W4A16_API int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches);
 
 
+/* Failure-detection self-test (the pages have no counterpart).  Enqueues
+ * one tiny kernel whose only wait can never be satisfied -- which = 0: an
+ * mbarrier phase that nothing completes; 1: a device word that nothing
+ * writes -- using the same bounded-wait helpers as every kernel of the
+ * library, with limit_cycles (1000 .. 2^31 SM cycles) in place of the
+ * library's limit of 2^31.  The wait gives up and records a timeout in the
+ * handle's status word; moe_w4a16_get_status then returns ERR_TIMEOUT (and
+ * clears it), and the context stays usable.  ERR_INVALID_ARG for a bad
+ * `which` or limit. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_selftest_timeout(moe_w4a16_handle* h, int32_t which,
+                                                          int64_t limit_cycles, moe_w4a16_stream_t stream);
+
 /* ======================================================================
  * Expert cache: the partial-residency miss path.
  *

@@ -479,3 +479,17 @@ const char* moe_w4a16_last_error(const moe_w4a16_handle* h) {
 }
 
 }  // extern "C"
+
+moe_w4a16_status moe_w4a16_selftest_timeout(moe_w4a16_handle* h, int32_t which, int64_t limit_cycles,
+                                            moe_w4a16_stream_t stream) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  if (which < 0 || which > 1) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (limit_cycles < 1000 || limit_cycles > (1ll << 31))
+    return fail(h, MOE_W4A16_ERR_INVALID_ARG, "limit_cycles outside [1000, 2^31]");
+  DeviceGuard dg(h->cfg.device);
+  if (!dg.ok) return fail(h, MOE_W4A16_ERR_CUDA, "cudaSetDevice failed");
+  const cudaError_t e = launch_selftest_wait(h->status, h->counters + never_set_word(h->cfg.hidden), which,
+                                             (long long)limit_cycles, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "selftest launch");
+  return MOE_W4A16_OK;
+}

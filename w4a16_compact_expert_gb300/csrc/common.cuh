@@ -100,16 +100,34 @@ DEV_INLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // one second), records STATUS_TIMEOUT and returns false.  No wait in this
 // library is unbounded.
 #define MOE_WAIT_CYCLES (1ll << 31)
-DEV_INLINE bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, DevStatus* st) {
+DEV_INLINE bool mbar_wait_limit(uint64_t* bar, uint32_t parity, DevStatus* st, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       atomicOr(&st->flags, STATUS_TIMEOUT);
       return false;
     }
   }
   return true;
+}
+DEV_INLINE bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, DevStatus* st) {
+  return mbar_wait_limit(bar, parity, st, MOE_WAIT_CYCLES);
+}
+
+// Bounded poll until *flag >= target (acquire loads); same give-up rule.
+DEV_INLINE bool flag_wait_limit(const unsigned* flag, unsigned target, DevStatus* st, long long limit) {
+  const long long t0 = clock64();
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) return true;
+    if (clock64() - t0 > limit) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      return false;
+    }
+    __nanosleep(256);
+  }
 }
 
 // 1-D bulk async copy global -> shared (TMA, no tensor map), completing on bar.

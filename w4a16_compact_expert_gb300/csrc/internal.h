@@ -56,7 +56,14 @@ struct FwdCtx {
 // barrier, [2, 2 + H/32) down arrival counters, then [2][256] per-expert
 // readiness counters.  Zero-initialised; every user leaves it zero (the grid
 // barrier: a multiple of the grid size).
-inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256; }
+inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256 + 1; }
+// the last word of the counter block: never written by any kernel (the
+// self-test waits on it)
+inline size_t never_set_word(int H) { return counter_words(H) - 1; }
+
+// selftest.cu: one kernel whose only wait can never be satisfied.
+cudaError_t launch_selftest_wait(DevStatus* st, const unsigned* never_set, int which, long long limit,
+                                 cudaStream_t s);
 
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* q, const uint16_t* s, uint8_t* slot_base,

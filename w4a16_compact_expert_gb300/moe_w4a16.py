@@ -27,7 +27,7 @@ EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "
             "moe_w4a16_cache_create", "moe_w4a16_cache_destroy", "moe_w4a16_cache_acquire",
             "moe_w4a16_cache_release", "moe_w4a16_cache_get_stats", "moe_w4a16_cache_slot_of",
             "moe_w4a16_cache_last_error", "moe_w4a16_cache_create_sim", "moe_w4a16_cache_sim_complete",
-            "moe_w4a16_cache_sim_fail"]
+            "moe_w4a16_cache_sim_fail", "moe_w4a16_selftest_timeout"]
 PATH_NONE, PATH_DECODE_FUSED, PATH_DECODE, PATH_GEMM = 0, 1, 2, 3
 PATH_NAMES = {PATH_NONE: "none", PATH_DECODE_FUSED: "decode_fused", PATH_DECODE: "decode", PATH_GEMM: "gemm"}
 
@@ -103,6 +103,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_cache_last_error.restype = ctypes.c_char_p
     lib.moe_w4a16_cache_sim_complete.argtypes = [vp, u64]
     lib.moe_w4a16_cache_sim_fail.argtypes = [vp, i32]
+    lib.moe_w4a16_selftest_timeout.argtypes = [vp, i32, ctypes.c_int64, vp]
     _lib = lib
     return lib
 
@@ -175,6 +176,10 @@ class MoELayer:
         n = ctypes.c_int32(0)
         p = self.lib.moe_w4a16_last_path(self.h, ctypes.byref(n))
         return int(p), int(n.value)
+
+    def selftest_timeout(self, which: int, limit_cycles: int, stream=None):
+        """Enqueue the failure-detection self-test (a wait that runs out)."""
+        self._check(self.lib.moe_w4a16_selftest_timeout(self.h, int(which), int(limit_cycles), _stream(stream)))
 
     # -- API
     def pack_experts(self, slot0: int, gate_q, gate_s, up_q, up_s, down_q, down_s, stream=None):
