@@ -72,6 +72,8 @@ def parse():
                     help="gemv: decode kernels (single launch when it fits); unfused: decode kernels as "
                          "separate launches; gemm: tensor-core grouped GEMM")
     ap.add_argument("--sweep", action="store_true", help="stack: T sweep with both kernel families")
+    ap.add_argument("--cache", action="store_true",
+                    help="qwen: partial residency through the expert cache (misses copied from host memory)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="layers (pools) per step")
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
@@ -567,6 +569,78 @@ def stack_sweep(args, rank, world, local_rank):
             "crossover_note": "smallest swept T at which the grouped GEMM is faster than the decode kernels"}
 
 
+def cache_bench(args, rank, world, local_rank):
+    """Qwen-shaped layer, 39 published slot rows over all 60 experts: each step
+    routes T tokens on the GPU, reads the ids, acquires the routed group
+    through the expert cache (misses stream from the host backing through
+    pinned staging), runs the forward and releases the lease."""
+    import numpy as np
+    import torch
+    from w4a16_compact_expert_gb300 import build_ext, moe_w4a16 as M, synth
+    build_ext.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    s, T = QWEN, tokens_of(args)
+    steps = args.steps or 200
+    rng = np.random.Generator(np.random.PCG64(synth.SEED_QWEN_PARTIAL))
+    E, H, I = s.E, s.H, s.I
+    backing = (rng.integers(0, 256, (E, I, H // 2), dtype=np.uint8),
+               (rng.uniform(0.002, 0.02, (E, I, s.nb_h)).astype(np.float16)).view(np.uint16),
+               rng.integers(0, 256, (E, I, H // 2), dtype=np.uint8),
+               (rng.uniform(0.002, 0.02, (E, I, s.nb_h)).astype(np.float16)).view(np.uint16),
+               rng.integers(0, 256, (E, H, I // 2), dtype=np.uint8),
+               (rng.uniform(0.002, 0.02, (E, H, s.nb_i)).astype(np.float16)).view(np.uint16))
+    group = min(E, T * s.k)
+    m = M.MoELayer(H, I, E, s.k, num_slots=s.slots + group, max_tokens=T, device=local_rank)
+    cache = M.ExpertCache(m, backing, staging_experts=4, spare_slots=group, max_group=group,
+                          initial=list(range(s.slots)))
+    g = torch.Generator(device=dev)
+    g.manual_seed(30_000)
+    rw = (torch.randn(E, H, device=dev, generator=g) * 0.02).half()
+    xs = [torch.randn(T, H, device=dev, generator=g).half() for _ in range(ROTATE)]
+    out = torch.empty(T, H, device=dev, dtype=torch.float16)
+
+    def one(i):
+        ids, _, _, _ = M.route_noalloc(xs[i % ROTATE], rw, None, E, s.k)
+        grp = sorted(set(ids.cpu().numpy().ravel().tolist()))
+        lease = cache.acquire(grp)
+        m.forward(xs[i % ROTATE], rw, None, 0, out=out)
+        cache.release(lease)
+
+    for i in range(max(3, args.warmup)):
+        one(i)
+    torch.cuda.synchronize()
+    s0 = cache.stats()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    s1 = cache.stats()
+    st, miss = m.get_status()
+    assert st == M.OK and miss == 0, (st, miss)
+    misses = s1["misses"] - s0["misses"]
+    hits = s1["hits"] - s0["hits"]
+    h2d = s1["h2d_bytes"] - s0["h2d_bytes"]
+    cfg = workload_config(args, T)
+    cfg["workload"] = (f"one Qwen-MoE-shaped layer (H={H} I={I} E={E} top-{s.k}), {s.slots} published slot rows over "
+                       f"all {E} experts through the expert cache, T={T} tokens per step")
+    cfg["layers_per_step"] = 1
+    cfg["l2"] = "misses copied from host memory; resident weights 171 MB"
+    res = {"metric": "MoE-layer tokens/s with the expert cache's miss path in the loop",
+           "value": T * steps * world / el, "unit": UNIT, "n_gpus": world, "steps": steps,
+           "ms_per_step": el * 1e3 / steps, "higher_is_better": True,
+           "config": cfg | {"path": "route + acquire + forward + release per step",
+                                                "published_rows": s.slots, "spare_rows": group,
+                                                "staging_experts": 4, "backing": "host memory, all 60 experts"},
+           "cache": {"misses_per_step": misses / steps, "hit_rate": hits / max(1, hits + misses),
+                     "h2d_gbs": h2d / el / 1e9, "d2h_bytes": s1["d2h_bytes"], "evictions": s1["evictions"],
+                     "lease_waits": s1["lease_waits"], "generation": s1["generation"]}}
+    cache.close()
+    m.close()
+    return res
+
+
 def main():
     args = parse()
     if args.cpu_leg:
@@ -596,6 +670,8 @@ def main():
         torch.distributed.init_process_group("nccl")
     if args.sweep:
         res = stack_sweep(args, rank, world, local_rank)
+    elif args.cache:
+        res = cache_bench(args, rank, world, local_rank)
     else:
         # CPU baseline first, in its own process, before this process touches the GPU.
         cpu = None

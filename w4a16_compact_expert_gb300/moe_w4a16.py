@@ -104,6 +104,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_cache_sim_complete.argtypes = [vp, u64]
     lib.moe_w4a16_cache_sim_fail.argtypes = [vp, i32]
     lib.moe_w4a16_selftest_timeout.argtypes = [vp, i32, ctypes.c_int64, vp]
+    lib.moe_w4a16_route_noalloc.argtypes = [vp, i32, i32, i32, i32, vp, vp, u32, vp, vp, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -238,6 +239,25 @@ class MoELayer:
         miss = ctypes.c_int64(0)
         st = self.lib.moe_w4a16_get_status(self.h, ctypes.byref(miss))
         return st, miss.value
+
+
+def route_noalloc(x, router_w, bias, num_experts: int, top_k: int, flags: int = 0, stream=None):
+    """Routing only, through moe_w4a16_route_noalloc (no handle, no device
+    allocation inside the library).  Returns device tensors (ids [T, k],
+    weights [T, k], sorted pairs [T*k], offsets [E+1])."""
+    import torch
+    lib = load_library()
+    T, H = x.shape
+    dev = x.device
+    ids = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+    sp = torch.empty((T * top_k,), dtype=torch.int32, device=dev)
+    off = torch.empty((num_experts + 1,), dtype=torch.int32, device=dev)
+    st = lib.moe_w4a16_route_noalloc(_ptr(x), T, H, num_experts, top_k, _ptr(router_w), _ptr(bias), flags,
+                                     _ptr(ids), _ptr(w), _ptr(sp), _ptr(off), _stream(stream))
+    if st != OK:
+        raise MoEError(st, lib.moe_w4a16_last_error(None).decode())
+    return ids, w, sp, off
 
 
 class ExpertCache:
