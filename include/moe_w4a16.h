@@ -170,7 +170,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_get_status(moe_w4a16_handle* h, int64_t
  * the message of the last failed create. */
 MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
 
-/* Limits of moe_w4a16_route_noalloc (its scratch is a fixed 4 MiB device array). */
+/* Limits of moe_w4a16_route_noalloc (its scratch is a fixed 5 MiB device array). */
 #define MOE_W4A16_NOALLOC_MAX_TOKENS 4096
 #define MOE_W4A16_NOALLOC_MAX_HIDDEN 4096
 #define MOE_W4A16_NOALLOC_MAX_LOGITS 786432   /* T * num_experts * ceil(hidden / 256) */
@@ -191,7 +191,7 @@ MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
  *   topk_ids [T][k] int32, topk_w [T][k] FP32: device outputs (required);
  *   sorted_pairs [T*k] int32, expert_offsets [E+1] int32: device outputs or NULL.
  * Work is enqueued on `stream` (the calling thread's current device).
- * Scratch lives in one file-scope device array of 4 MiB that every device
+ * Scratch lives in one file-scope device array of 5 MiB that every device
  * which loads the library keeps until the process exits.  The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture on the device.
@@ -232,8 +232,8 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h
  * how many kernels it launched (debug-output copies not counted):
  *   MOE_W4A16_PATH_DECODE_FUSED  1 cooperative kernel (routing, permutation,
  *                                gate/up, down and combine in one launch)
- *   MOE_W4A16_PATH_DECODE        router (1 or 3 kernels) + gate/up + down
- *   MOE_W4A16_PATH_GEMM          router (1 or 3) + gather + gate/up GEMM +
+ *   MOE_W4A16_PATH_DECODE        router (1 or 4 kernels) + gate/up + down
+ *   MOE_W4A16_PATH_GEMM          router (1 or 4) + gather + gate/up GEMM +
  *                                down GEMM + combine
  * PATH_NONE before any forward and after one with T == 0.  *launches may be
  * NULL.  Returns -1 for a NULL handle. */

@@ -182,6 +182,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   ALLOC(h->sorted, P);
   ALLOC(h->p2r, P);
   ALLOC(h->act, 5 * E + 2 + 1);
+  ALLOC(h->route_hist, (size_t)((T + 7) / 8) * E);
   ALLOC(h->xp, P * H);
   ALLOC(h->hbuf, P * I);
   ALLOC(h->ybuf, P * H);
@@ -345,6 +346,8 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.xp = h->xp;
   c.hbuf = h->hbuf;
   c.ybuf = h->ybuf;
+  c.route_hist = h->route_hist;
+  c.route_counter = h->counters + route_counter_word(h->cfg.hidden);
   c.grid_bar = reinterpret_cast<unsigned long long*>(h->counters);
   c.down_counters = h->counters + 2;
   c.expert_ready = h->counters + 2 + h->cfg.hidden / 32;
@@ -395,7 +398,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
-  const int route_launches = fused_route && route_single_launch(c) ? 1 : 3;
+  const int route_launches = fused_route && route_single_launch(c) ? 1 : 4;
   int32_t path = gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
   if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);

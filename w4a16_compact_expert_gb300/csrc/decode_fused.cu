@@ -772,36 +772,37 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
         }
       }
       const int kc0 = wq * nkh / GW, kc1 = (wq + 1) * nkh / GW;   // the warp's K chunks
-      float acc[2][2][4];
+      float* rw = rg + wq * 2 * 16 * ntok;   // K-split partials -> rg[warp][mat][row][token]
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
+        float acc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) acc[mat][nt][r] = 0.f;
+          for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
         const int e = 2 * i + mat, s = e % NS;
         warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
         const uint8_t* tile = sm + (size_t)s * L.slot_bytes;
         if (ntl == 1)
-          mma_range<1>(acc[mat], tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
+          mma_range<1>(acc, tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
         else
-          mma_range<2>(acc[mat], tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with the entry
-      }
-      // K-split partials -> rg[warp][mat][row][token]
-      float* rw = rg + wq * 2 * 16 * ntok;
-#pragma unroll
-      for (int mat = 0; mat < 2; ++mat)
+          mma_range<2>(acc, tile, c.lay.gate.scale_bytes, brow, pre, lane, kc0, kc1);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
           if (nt < ntl) {
             float* r0 = rw + (mat * 16 + g) * ntok + nt * 8 + 2 * cc;
-            r0[0] = acc[mat][nt][0];
-            r0[1] = acc[mat][nt][1];
-            r0[8 * ntok] = acc[mat][nt][2];
-            r0[8 * ntok + 1] = acc[mat][nt][3];
+            r0[0] = acc[nt][0];
+            r0[1] = acc[nt][1];
+            r0[8 * ntok] = acc[nt][2];
+            r0[8 * ntok + 1] = acc[nt][3];
           }
+        // The entry is released only after stores that depend on every word
+        // read from it: the shared loads have completed before the bulk copy
+        // that refills the slot can be issued.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
       named_sync(gbar, GW * 32);
       for (int idx = gtid; idx < 16 * cnt; idx += GW * 32) {
         const int tok = idx >> 4, row = idx & 15;
@@ -871,6 +872,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
           c.ybuf[(size_t)r_sorted[start + p0 + tok] * H + hb * kDownRows + row] = y;
         }
       }
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }

@@ -317,8 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* raw = smem + C::kOffRaw + rr.i * C::kRawBytes;
 #pragma unroll
         for (int m = 0; m < C::kMats; ++m) q[m][0] = *reinterpret_cast<const uint4*>(raw + (m * 8 + warp) * 512 + lane * 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rr.i]);
         if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
           ok = false;
           break;
@@ -346,7 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[ra.i]);
+        // The raw slot is released only now, after its words were consumed by
+        // the arithmetic above: an arrive issued right behind the shared loads
+        // let the next TMA fill overtake loads still queued behind the tensor
+        // core's shared-memory traffic (seen as a few corrupt weight rows in
+        // about one forward in twenty-five of the MMA-bound down projection).
+        if (lane == 0) {
+          mbar_arrive(&a_full[ra.i]);
+          mbar_arrive(&raw_empty[rr.i]);
+        }
         rr.next(C::kStagesRaw);
         ra.next(kStagesA);
       }

@@ -33,6 +33,7 @@ struct moe_w4a16_handle {
   int32_t* sorted = nullptr;
   int32_t* p2r = nullptr;
   int32_t* act = nullptr;            // 5 arrays of E (+1) ints, see fill_ctx
+  int32_t* route_hist = nullptr;     // [ceil(max_tokens/8)][E]
   __half* xp = nullptr;
   __half* hbuf = nullptr;
   float* ybuf = nullptr;

@@ -44,6 +44,8 @@ struct FwdCtx {
   __half* xp;                  // [T*k][H] activations gathered in sorted-row order (prefill)
   __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
+  int32_t* route_hist;         // [ceil(T/8)][E] per 8-token block expert counts, then bases (large-T router)
+  unsigned* route_counter;     // [1] arrival counter of the large-T router's scan (self-resetting)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
   unsigned long long* grid_bar;  // grid-barrier arrivals (monotonic, a multiple of the grid between uses)
   unsigned* expert_ready;      // [2][256] per active expert: finished gate/up items, started down items
@@ -56,7 +58,9 @@ struct FwdCtx {
 // barrier, [2, 2 + H/32) down arrival counters, then [2][256] per-expert
 // readiness counters.  Zero-initialised; every user leaves it zero (the grid
 // barrier: a multiple of the grid size).
-inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256 + 1; }
+inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256 + 2; }
+// the word after the readiness counters: the large-T router's arrival counter
+inline size_t route_counter_word(int H) { return 2 + (size_t)H / 32 + 2 * 256; }
 // the last word of the counter block: never written by any kernel (the
 // self-test waits on it)
 inline size_t never_set_word(int H) { return counter_words(H) - 1; }

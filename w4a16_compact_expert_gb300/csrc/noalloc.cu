@@ -13,7 +13,7 @@
 #include "moe_w4a16.h"
 #include "internal.h"
 
-#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (5u << 20)
 
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
@@ -35,7 +35,10 @@ constexpr size_t kOffOffsets = kOffP2r + (size_t)kMaxPairs * 4;     // [E+1] i32
 constexpr size_t kOffAct = kOffOffsets + 2048;                      // 5E+2 i32: active-expert lists
 constexpr size_t kOffTable = kOffAct + 8192;                        // [E] i32 identity expert->slot
 constexpr size_t kOffStatus = kOffTable + 1024;                     // DevStatus
-constexpr size_t kOffEnd = kOffStatus + 256;
+constexpr size_t kOffCounter = kOffStatus + 256;                    // u32 arrival counter of the router scan
+constexpr size_t kOffHist = kOffCounter + 256;                      // [ceil(T/8)][E] i32 block counts
+constexpr size_t kMaxHist = (size_t)kMaxLogits / 8 + kMaxE;         // ceil(T/8) * E <= T*E/8 + E
+constexpr size_t kOffEnd = kOffHist + kMaxHist * 4;
 static_assert(kOffEnd <= MOE_NOALLOC_SCRATCH_BYTES, "scratch layout exceeds the static array");
 static_assert((kMaxE + 1) * 4 <= 2048 && (5 * kMaxE + 2) * 4 <= 8192 && kMaxE * 4 <= 1024, "scratch slots");
 
@@ -51,6 +54,7 @@ __global__ void noalloc_prepare_kernel(int E) {
     DevStatus* s = reinterpret_cast<DevStatus*>(g_route_scratch + kOffStatus);
     s->miss = 0;
     s->flags = 0;
+    *reinterpret_cast<unsigned*>(g_route_scratch + kOffCounter) = 0u;
   }
 }
 
@@ -129,6 +133,8 @@ extern "C" MOE_W4A16_API moe_w4a16_status moe_w4a16_route_noalloc(
   c.n_active = act + 5 * num_experts + 1;
   c.tile_tokens = 128;
   c.status = reinterpret_cast<DevStatus*>(base + kOffStatus);
+  c.route_counter = reinterpret_cast<unsigned*>(base + kOffCounter);
+  c.route_hist = reinterpret_cast<int32_t*>(base + kOffHist);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   noalloc_prepare_kernel<<<1, 256, 0, st>>>(num_experts);
   e = cudaGetLastError();

@@ -212,65 +212,165 @@ __global__ void __launch_bounds__(128) route_logits_mma_kernel(FwdCtx c) {
 }
 
 // One warp per token: sums the K slices of its logits (fixed order), then
-// softmax / top-k.
+// softmax / top-k; then the CTA counts its 8 tokens' pairs per expert
+// (route_hist row = blockIdx.x) for the parallel permutation.
 __global__ void __launch_bounds__(256) route_topk_kernel(FwdCtx c) {
   __shared__ float lg[8][256];
+  __shared__ int hcount[256];
   pdl_wait();
   pdl_trigger();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + w;
-  if (t >= c.T) return;
-  for (int e = lane; e < c.E; e += 32) {
-    float s = 0.f;
-    for (int ks0 = 0; ks0 < c.ksplit; ks0 += 8) {   // 8 independent loads in flight, summed in order
-      float v[8];
+  for (int e = threadIdx.x; e < c.E; e += blockDim.x) hcount[e] = 0;
+  if (t < c.T) {
+    for (int e = lane; e < c.E; e += 32) {
+      float s = 0.f;
+      for (int ks0 = 0; ks0 < c.ksplit; ks0 += 8) {   // 8 independent loads in flight, summed in order
+        float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[i] = ks0 + i < c.ksplit ? c.logit_part[((size_t)(ks0 + i) * c.T + t) * c.E + e] : 0.f;
+        for (int i = 0; i < 8; ++i)
+          v[i] = ks0 + i < c.ksplit ? c.logit_part[((size_t)(ks0 + i) * c.T + t) * c.E + e] : 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += v[i];
+        for (int i = 0; i < 8; ++i) s += v[i];
+      }
+      lg[w][e] = s;
     }
-    lg[w][e] = s;
+    float r = 1.f;
+    if (c.flags & 2u) {
+      float ss = 0.f;
+      for (int ks = 0; ks < c.ksplit; ++ks) ss += c.ss_part[(size_t)ks * c.T + t];
+      r = prenorm_scale(ss, c.H);
+      if (lane == 0) c.rnorm[t] = r;
+    }
+    __syncwarp();
+    topk_token(c, t, lg[w], r, nullptr);
   }
-  float r = 1.f;
-  if (c.flags & 2u) {
-    float ss = 0.f;
-    for (int ks = 0; ks < c.ksplit; ++ks) ss += c.ss_part[(size_t)ks * c.T + t];
-    r = prenorm_scale(ss, c.H);
-    if (lane == 0) c.rnorm[t] = r;
-  }
-  __syncwarp();
-  topk_token(c, t, lg[w], r, nullptr);
+  __syncthreads();   // this CTA's ids (global) are visible to the whole CTA
+  const int p0 = blockIdx.x * 8 * c.k, p1 = min(c.T, blockIdx.x * 8 + 8) * c.k;
+  for (int p = p0 + (int)threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hcount[c.ids[p]], 1);   // counts: order-free
+  __syncthreads();
+  for (int e = threadIdx.x; e < c.E; e += blockDim.x) c.route_hist[(size_t)blockIdx.x * c.E + e] = hcount[e];
 }
 
-// One CTA: the expert ids are staged in shared memory (one byte each), then
-// histogram, scan and stable scatter run out of shared memory.
-__global__ void __launch_bounds__(1024) route_permute_kernel(FwdCtx c, int ids_in_smem) {
-  extern __shared__ __align__(16) int perm_smem[];
+// One CTA per expert: exclusive scan of the expert's counts over the 8-token
+// blocks (in place: route_hist becomes the block's first row inside the
+// expert's group) and the expert's total in offsets[e].  The last CTA to
+// finish (arrival counter) turns the totals into the exclusive offsets and
+// the active-expert lists of the grouped GEMM, and resets the counter.
+__global__ void __launch_bounds__(256) route_scan_kernel(FwdCtx c) {
+  __shared__ int warp_tot[8];
+  __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
-  const int P = c.T * c.k;
-  if (ids_in_smem) {
-    uint8_t* ids8 = reinterpret_cast<uint8_t*>(perm_smem);
-    int* scratch = perm_smem + (P + 15) / 16 * 4;
-    // 16 independent loads in flight per thread before any store
-    for (int p0 = 0; p0 < P; p0 += 16 * 1024) {
-      int v[16];
+  const int e = blockIdx.x, nb = (c.T + 7) / 8;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int per = (nb + 255) / 256;   // consecutive blocks per thread
+  const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+  int loc = 0;
+  for (int bb = b0; bb < b1; ++bb) loc += c.route_hist[(size_t)bb * c.E + e];
+  int incl = loc;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int p = p0 + i * 1024 + threadIdx.x;
-        v[i] = p < P ? c.ids[p] : 0;
-      }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int ww = 0; ww < w; ++ww) before += warp_tot[ww];
+  int run = before + incl - loc;   // exclusive prefix of this thread's first block
+  for (int bb = b0; bb < b1; ++bb) {
+    const int v = c.route_hist[(size_t)bb * c.E + e];
+    c.route_hist[(size_t)bb * c.E + e] = run;
+    run += v;
+  }
+  if (tid == 255) c.offsets[e] = before + incl;   // the expert's total (the last thread holds it)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(c.route_counter, 1u) == (unsigned)c.E - 1u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (w == 0) {   // totals -> exclusive offsets, active lists (ascending experts)
+    int n = 0, tiles = 0, base = 0;
+    for (int e0 = 0; e0 < c.E; e0 += 32) {
+      const int ex = e0 + lane;
+      const int ce = ex < c.E ? __ldcg(&c.offsets[ex]) : 0;
+      int ci = ce;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int p = p0 + i * 1024 + threadIdx.x;
-        if (p < P) ids8[p] = (uint8_t)v[i];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, ci, o);
+        if (lane >= o) ci += v;
       }
+      const int off = base + ci - ce;
+      const int slot = ce > 0 ? c.table[ex] : -1;
+      const bool act = ce > 0 && slot >= 0;
+      if (ce > 0 && slot < 0) {
+        atomicAdd(&c.status->miss, (unsigned long long)ce);
+        atomicOr(&c.status->flags, STATUS_MISS);
+      }
+      const unsigned am = __ballot_sync(kFull, act);
+      const int pos = n + __popc(am & ((1u << lane) - 1u));
+      const int ntl = act ? (ce + c.tile_tokens - 1) / c.tile_tokens : 0;
+      int ti = ntl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, ti, o);
+        if (lane >= o) ti += v;
+      }
+      __syncwarp();
+      if (ex < c.E) c.offsets[ex] = off;
+      if (act) {
+        c.act_expert[pos] = ex;
+        c.act_slot[pos] = slot;
+        c.act_start[pos] = off;
+        c.act_count[pos] = ce;
+        c.act_tile[pos] = tiles + ti - ntl;
+      }
+      n += __popc(am);
+      tiles += __shfl_sync(kFull, ti, 31);
+      base += __shfl_sync(kFull, ci, 31);
     }
-    __syncthreads();
-    permute_block(c, ids8, scratch);
-  } else {
-    permute_block(c, c.ids, perm_smem);
+    if (lane == 0) {
+      c.offsets[c.E] = base;
+      *c.n_active = n;
+      c.act_tile[n] = tiles;
+      *c.route_counter = 0u;
+    }
+  }
+}
+
+// One CTA per 8-token block: stable scatter of its pairs.  The rank of a pair
+// inside its expert group = the block's base (route_hist) + the pairs of the
+// same expert earlier in the block (__match_any_sync per 32 pairs, then the
+// counts of the earlier 32-pair chunks).
+__global__ void __launch_bounds__(256) route_scatter_kernel(FwdCtx c) {
+  __shared__ int ccount[8][256];   // [32-pair chunk][expert]
+  pdl_wait();
+  pdl_trigger();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p0 = blockIdx.x * 8 * c.k, p1 = min(c.T, blockIdx.x * 8 + 8) * c.k;
+  const int nch = (p1 - p0 + 31) / 32;   // <= 8 (k <= 32)
+  for (int i = threadIdx.x; i < nch * c.E; i += blockDim.x) ccount[i / c.E][i % c.E] = 0;
+  __syncthreads();
+  int e = -1 - lane, rank = 0;
+  unsigned peers = 0;
+  const int p = p0 + w * 32 + lane;
+  if (w < nch) {
+    e = p < p1 ? c.ids[p] : -1 - lane;
+    peers = __match_any_sync(kFull, e);
+    rank = __popc(peers & ((1u << lane) - 1u));
+    if (p < p1 && rank == 0) ccount[w][e] = __popc(peers);
+  }
+  __syncthreads();
+  if (w < nch && p < p1) {
+    int r = rank;
+    for (int ch = 0; ch < w; ++ch) r += ccount[ch][e];
+    const int pos = c.offsets[e] + c.route_hist[(size_t)blockIdx.x * c.E + e] + r;
+    c.sorted[pos] = p;
+    c.p2r[p] = pos;
   }
 }
 
@@ -295,12 +395,7 @@ cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
   const dim3 grid((c.T + kRouteTile - 1) / kRouteTile, (c.E + kRouteTile - 1) / kRouteTile, cc.ksplit);
   e = launch_pdl(route_logits_mma_kernel, grid, dim3(128), lsmem, st, 1, cc);
   if (e == cudaSuccess) e = launch_pdl(route_topk_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, cc);
-  const int P = c.T * c.k;
-  const size_t scratch = (size_t)(32 * c.E + 2 * c.E + 1) * sizeof(int);
-  const size_t smem_ids = (size_t)(P + 15) / 16 * 16 + scratch;
-  const int in_smem = smem_ids <= 200 * 1024;
-  const size_t smem = in_smem ? smem_ids : scratch;
-  if (e == cudaSuccess) e = opt_in_smem((const void*)route_permute_kernel, smem);
-  if (e == cudaSuccess) e = launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, st, 1, cc, in_smem);
+  if (e == cudaSuccess) e = launch_pdl(route_scan_kernel, dim3(c.E), dim3(256), 0, st, 1, cc);
+  if (e == cudaSuccess) e = launch_pdl(route_scatter_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, cc);
   return e;
 }
