@@ -5,8 +5,8 @@
 // design is not published).
 //
 // Grid = one CTA per SM, all co-resident (cooperative launch).  A CTA has 12
-// compute warps in NG groups of GW (3 x 4 for T <= 8, 2 x 6 above), one
-// producer warp and one signaller warp.
+// compute warps in NG groups of GW (6 x 2 for T <= 2, 3 x 4 for T <= 8, 2 x 6
+// above), one producer warp and one signaller warp.
 //   routing  the grid's warps take the (token, expert, K half) dot products
 //            of the router (and per-token sums of squares for PRENORM) ->
 //            global; one bounded grid barrier; then every CTA reads the logits
@@ -58,7 +58,9 @@ constexpr int kMaxExperts = 256;               // readiness counters per handle
 constexpr uint32_t kSmemBudget = 226 * 1024;
 
 // warps per compute group for a batch of T tokens
-__host__ __device__ inline int fused_group_warps(int T) { return T <= 8 ? 4 : 6; }
+// (2-warp groups give the most items in flight for one or two tokens; from 3
+// tokens on, fewer and wider groups spend less on the cross-warp reductions)
+__host__ __device__ inline int fused_group_warps(int T) { return T <= 2 ? 2 : T <= 8 ? 4 : 6; }
 
 struct FusedSmem {
   uint32_t ns, slot_bytes, off_x, off_h, off_red, off_sb, off_route, total;
@@ -67,8 +69,8 @@ struct FusedSmem {
 // Shared memory of the fused kernel for T tokens, top-k: the ring (as many
 // entries as fit, at most kMaxSlots), the x rows [T][H + 8], per-group h rows
 // [min(T, 8)][I + 8], the cross-warp reduction buffer and the routing state.
-__host__ __device__ inline FusedSmem fused_smem(const SlotLayout& lay, int H, int I, int E, int T, int k) {
-  const int NG = kCW / fused_group_warps(T);
+__host__ __device__ inline FusedSmem fused_smem(const SlotLayout& lay, int H, int I, int E, int T, int k, int gw) {
+  const int NG = kCW / gw;
   FusedSmem f;
   const uint32_t sg = lay.gate.tile_bytes, sd = 2 * lay.down.tile_bytes;
   f.slot_bytes = ((sg > sd ? sg : sd) + 127) / 128 * 128;
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const int T = c.T, E = c.E, H = c.H, I = c.I, k = c.k, P = T * k;
-  const FusedSmem L = fused_smem(c.lay, H, I, E, T, k);
+  const FusedSmem L = fused_smem(c.lay, H, I, E, T, k, GW);
   __half* xcache = reinterpret_cast<__half*>(sm + L.off_x);
   __half* hstage = reinterpret_cast<__half*>(sm + L.off_h);
   float* red = reinterpret_cast<float*>(sm + L.off_red);
@@ -743,7 +745,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   const int q = warp / GW, wq = warp % GW;   // group, warp in group
   const int gtid = tid - q * GW * 32;        // thread index inside the group
   const int g = lane >> 2, cc = lane & 3;
-  const int gbar = 2 + q;                    // named barrier of group q
+  const int gbar = 7 + q;                    // named barrier of group q (7 .. 12)
   const int ntok = T <= 8 ? 8 : 16;
   float* rg = red + q * GW * 2 * 16 * ntok;  // this group's reduction buffer
   __half* hs = hstage + (size_t)q * (T < kTok ? T : kTok) * (I + 8);   // this group's h rows
@@ -925,13 +927,14 @@ cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
 // kMinSlots weight entries.
 bool fused_decode_supported(const FwdCtx& c, int max_smem) {
   if (c.T > kMaxT || c.T * c.k > kMaxP || c.H % 64 || c.I % 64 || c.k > 32 || c.E > kMaxExperts) return false;
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T));
   return L.ns >= (uint32_t)kMinSlots && L.total <= kSmemBudget && (int)L.total <= max_smem;
 }
 
 cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k);
-  cudaError_t e = fused_group_warps(c.T) == 4 ? launch_fused<4>(c, L, st) : launch_fused<6>(c, L, st);
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T));
+  const int gw = fused_group_warps(c.T);
+  cudaError_t e = gw == 2 ? launch_fused<2>(c, L, st) : gw == 4 ? launch_fused<4>(c, L, st) : launch_fused<6>(c, L, st);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
