@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);   // one arrive per epilogue warp
+      mbar_init(&acc_empty[s], GU ? 12 : 4);   // one arrive per warp that reads the accumulator
     }
     fence_mbar_init();
   }
@@ -191,6 +191,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / kMTile;
   const uint32_t TS = LA.tile_bytes, SB = LA.scale_bytes;
   const int nacc = GU ? 1 : 2;   // accumulator buffers (gate/up uses all 512 columns)
+  // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
+  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32).
+  // Gate/up keeps a single accumulator, so its epilogue is on the MMA's
+  // critical path: it is split over the 4 epilogue warps and the 8 dequant
+  // warps (which wait for the MMA at that point anyway), a third each.
+  auto epilogue_chunks = [&](const Tile& et, uint32_t acc_col, int ch0, int ch1) {
+    const int qw = warp & 3, row = qw * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16) + acc_col;
+    for (int col0 = ch0 * 32; col0 < ch1 * 32 && col0 < et.n; col0 += 32) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(taddr + col0, va);
+      if (GU) tmem_ld32(taddr + 256u + col0, vb);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int nn = col0 + j;
+        if (nn < et.n) {
+          if (GU) {
+            float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
+            if (c.flags & 2u) {
+              const float r = c.rnorm[c.sorted[et.r0 + nn] / c.k];
+              gv *= r;
+              uv *= r;
+            }
+            c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
+          } else {
+            const int pair = c.sorted[et.r0 + nn];
+            c.ybuf[(size_t)pair * c.H + et.m0 + row] = __uint_as_float(va[j]);
+          }
+        }
+      }
+    }
+  };
 
   if (warp == kWarpProd) {
     // ------------------------------------------------- int4 chunk producer
@@ -281,8 +314,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kDqWarps) {
     // ------------------------------------------------------------ dequant
     const int g = lane >> 2, cq = lane & 3;
-    Ring rr, ra;
+    Ring rr, ra, racc;
     bool ok = true;
+    Tile pend;               // gate/up: the tile whose epilogue share is still due
+    bool have = false;
+    // this warp's third of a gate/up tile's epilogue (warps 0-3 the middle,
+    // 4-7 the last third of the 32-column chunks)
+    auto epilogue_share = [&]() -> bool {
+      if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) return false;
+      tc_fence_after();
+      const int nch = (pend.n + 31) / 32, part = 1 + (warp >> 2);
+      epilogue_chunks(pend, 0u, part * nch / 3, (part + 1) * nch / 3);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
+      racc.next(1);
+      have = false;
+      return true;
+    };
     for (int t = blockIdx.x; ok; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, tl)) break;
@@ -301,6 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       load_scales(0, nlo, nhi);
       for (int ks = 0; ks < nks; ++ks) {
+        // the A ring is full at this point: the MMA waits for the previous
+        // tile's epilogue before it takes stage 0 of this one
+        if (GU && have && ks == kStagesA && !epilogue_share()) {
+          ok = false;
+          break;
+        }
         if ((ks & 3) == 0) {
 #pragma unroll
           for (int m = 0; m < C::kMats; ++m) {
@@ -356,42 +411,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         rr.next(C::kStagesRaw);
         ra.next(kStagesA);
       }
+      if (GU && ok) {
+        pend = tl;
+        have = true;
+      }
     }
+    if (GU && ok && have) epilogue_share();   // the last tile
   } else {
     // ----------------------------------------------------------- epilogue
-    const int qw = warp & 3;   // warps 8..11 -> TMEM lane quarters 0..3
-    const int row = qw * 32 + lane;
+    // warps 8..11 -> TMEM lane quarters 0..3
     Ring racc;
     for (int t = blockIdx.x;; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, tl)) break;
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16) + (GU ? 0u : (uint32_t)racc.i * 256u);
-      for (int col0 = 0; col0 < tl.n; col0 += 32) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(taddr + col0, va);
-        if (GU) tmem_ld32(taddr + 256u + col0, vb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int nn = col0 + j;
-          if (nn < tl.n) {
-            if (GU) {
-              float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
-              if (c.flags & 2u) {
-                const float r = c.rnorm[c.sorted[tl.r0 + nn] / c.k];
-                gv *= r;
-                uv *= r;
-              }
-              c.hbuf[(size_t)(tl.r0 + nn) * c.I + tl.m0 + row] = __float2half_rn(silu_mul(gv, uv));
-            } else {
-              const int pair = c.sorted[tl.r0 + nn];
-              c.ybuf[(size_t)pair * c.H + tl.m0 + row] = __uint_as_float(va[j]);
-            }
-          }
-        }
-      }
+      const int nch = (tl.n + 31) / 32;
+      epilogue_chunks(tl, GU ? 0u : (uint32_t)racc.i * 256u, 0, GU ? nch / 3 : nch);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
