@@ -46,7 +46,10 @@ struct Cfg {
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
   static constexpr int kBBytes = kNMax * kBK * 2;         // 32 KB
-  static constexpr int kRawBytes = kMats * 8 * 512;       // int4 chunks of 8 row tiles
+  // int4 chunks of 8 row tiles per matrix, then (at block boundaries) the
+  // 16 block scales of the same 8 row tiles per matrix
+  static constexpr int kRawQ = kMats * 8 * 512;
+  static constexpr int kRawBytes = kRawQ + kMats * 8 * 32;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStagesA * kABytes;
   static constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
@@ -141,7 +144,8 @@ DEV_INLINE void st_shared_v2_b32(uint32_t addr, uint32_t v0, uint32_t v1) {
 template <bool GU>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(FwdCtx c, const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
-                        const __grid_constant__ CUtensorMap tmA1) {
+                        const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmS0,
+                        const __grid_constant__ CUtensorMap tmS1) {
   using C = Cfg<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -189,7 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const MatLayout& LA = GU ? c.lay.gate : c.lay.down;
   const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / kMTile;
-  const uint32_t TS = LA.tile_bytes, SB = LA.scale_bytes;
   const int nacc = GU ? 1 : 2;   // accumulator buffers (gate/up uses all 512 columns)
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
   // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32).
@@ -239,9 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* dst = smem + C::kOffRaw + rr.i * C::kRawBytes;
-          mbar_expect_tx(&raw_full[rr.i], C::kRawBytes);
+          const bool blk = (ks & 3) == 0;   // first K step of a scale block: its scales come along
+          mbar_expect_tx(&raw_full[rr.i], blk ? (uint32_t)C::kRawBytes : (uint32_t)C::kRawQ);
           tma_load_4d(dst, &tmA0, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
           if (GU) tma_load_4d(dst + 8 * 512, &tmA1, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+          if (blk) {
+            tma_load_4d(dst + C::kRawQ, &tmS0, 0, ks >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+            if (GU) tma_load_4d(dst + C::kRawQ + 256, &tmS1, 0, ks >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+          }
           rr.next(C::kStagesRaw);
         }
         if (!ok) break;
@@ -335,20 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; ok; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, tl)) break;
-      const uint8_t* base = c.pool + (size_t)tl.slot * c.slot_bytes;
-      // Scales of the thread's rows: block b in use, block b+1 prefetched.
+      // the scales of the thread's rows for the current block (read from the
+      // raw stage that starts the block)
       __half2 slo[2][1], shi[2][1];
-      __half nlo[2][1], nhi[2][1];
-      auto load_scales = [&](int b, __half (&lo)[2][1], __half (&hi)[2][1]) {
-#pragma unroll
-        for (int m = 0; m < C::kMats; ++m) {
-          const MatLayout& L = (GU && m == 1) ? c.lay.up : LA;
-          const __half* sc = reinterpret_cast<const __half*>(base + L.off + (size_t)(tl.m0 / 16 + warp) * TS) + b * 16;
-          lo[m][0] = sc[g];
-          hi[m][0] = sc[g + 8];
-        }
-      };
-      load_scales(0, nlo, nhi);
       for (int ks = 0; ks < nks; ++ks) {
         // the A ring is full at this point: the MMA waits for the previous
         // tile's epilogue before it takes stage 0 of this one
@@ -356,20 +353,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if ((ks & 3) == 0) {
-#pragma unroll
-          for (int m = 0; m < C::kMats; ++m) {
-            slo[m][0] = __half2half2(nlo[m][0]);
-            shi[m][0] = __half2half2(nhi[m][0]);
-          }
-          if ((ks >> 2) + 1 < (int)LA.nb) load_scales((ks >> 2) + 1, nlo, nhi);
-        }
         if (!mbar_wait_bounded(&raw_full[rr.i], rr.ph, c.status)) {
           ok = false;
           break;
         }
         uint4 q[2][1];
         const uint8_t* raw = smem + C::kOffRaw + rr.i * C::kRawBytes;
+        if ((ks & 3) == 0) {
+#pragma unroll
+          for (int m = 0; m < C::kMats; ++m) {
+            const __half* sc = reinterpret_cast<const __half*>(raw + C::kRawQ + m * 256 + warp * 32);
+            slo[m][0] = __half2half2(sc[g]);
+            shi[m][0] = __half2half2(sc[g + 8]);
+          }
+        }
 #pragma unroll
         for (int m = 0; m < C::kMats; ++m) q[m][0] = *reinterpret_cast<const uint4*>(raw + (m * 8 + warp) * 512 + lane * 16);
         if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
@@ -579,6 +576,14 @@ PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slot
            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return pm;
+    // [slot][row tile][block][16 FP16 scales], the 16 scales of block b of 8 row tiles per load
+    const cuuint64_t sdims[4] = {16, L.nb, L.rows / 16, (cuuint64_t)num_slots};
+    const cuuint64_t sstrides[3] = {32, L.tile_bytes, lay.bytes};
+    const cuuint32_t sbox[4] = {16, 1, 8, 1};
+    if (fn(&pm.sc[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<uint8_t*>(pool + L.off), sdims, sstrides, sbox,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return pm;
   }
   pm.ok = true;
   return pm;
@@ -597,11 +602,11 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
   e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess)
     e = launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
-                   pm.q[1]);
+                   pm.q[1], pm.sc[0], pm.sc[1]);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess)
     e = launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh, pm.q[2],
-                   pm.q[2]);
+                   pm.q[2], pm.sc[2], pm.sc[2]);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c);

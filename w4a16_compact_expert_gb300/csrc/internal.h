@@ -94,11 +94,13 @@ cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEve
 // gemm_tc.cu: prefill regime (gather, gate/up GEMM, down GEMM, combine)
 bool gemm_shapes_supported(int H, int I);
 
-// TMA descriptors of the compact int4 chunks of gate, up and down over the
-// whole slot pool (4-D: 512-byte chunk, K chunk, row tile, slot).  Built once
-// per handle.
+// TMA maps over the whole slot pool for the grouped GEMM, built once per
+// handle: q, the packed int4 chunks of gate, up and down ([slot][row tile][K
+// chunk][512 B]), and sc, their block scales ([slot][row tile][block][16
+// FP16]), boxes of 8 row tiles.
 struct PoolMaps {
   CUtensorMap q[3];
+  CUtensorMap sc[3];
   bool ok;
 };
 PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slots);
