@@ -31,18 +31,18 @@ namespace {
 constexpr int kMTile = 128;     // weight rows per tile (MMA M)
 constexpr int kNMax = 256;      // tokens per tile (MMA N, max)
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of FP16)
-constexpr int kStagesA = 3;
 constexpr int kDqWarps = 8;     // warps 0-7 dequant (one 16-row tile each)
 constexpr int kThreads = 480;   // + warps 8-11 epilogue, 12 int4 producer, 13 token producer, 14 MMA
-constexpr int kWarpEpi = 8, kWarpProd = 12, kWarpProdB = 13, kWarpMma = 14;
+constexpr int kWarpProd = 12, kWarpProdB = 13, kWarpMma = 14;   // warps 8-11: epilogue
 constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;
 
 template <bool GU>
 struct Cfg {
   static constexpr int kMats = GU ? 2 : 1;
-  static constexpr int kStagesB = GU ? 2 : 4;
-  static constexpr int kStagesRaw = GU ? 6 : 10;   // int4 chunks come from HBM: deepest ring
+  static constexpr int kStagesA = 3;             // dequantised FP16 A stages
+  static constexpr int kStagesB = GU ? 3 : 4;
+  static constexpr int kStagesRaw = GU ? 3 : 10;   // int4 chunks (+ scales) from HBM
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
   static constexpr int kBBytes = kNMax * kBK * 2;         // 32 KB
@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + C::kStagesRaw;
   uint64_t* a_full = raw_empty + C::kStagesRaw;
-  uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* b_full = a_empty + kStagesA;
+  uint64_t* a_empty = a_full + C::kStagesA;
+  uint64_t* b_full = a_empty + C::kStagesA;
   uint64_t* b_empty = b_full + C::kStagesB;
   uint64_t* acc_full = b_empty + C::kStagesB;   // [2]
   uint64_t* acc_empty = acc_full + 2;           // [2]
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kDqWarps);
     }
-    for (int s = 0; s < kStagesA; ++s) {
+    for (int s = 0; s < C::kStagesA; ++s) {
       mbar_init(&a_full[s], kDqWarps);
       mbar_init(&a_empty[s], 1);
     }
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(&a_empty[ra.i]);
           umma_commit(&b_empty[rb.i]);
-          ra.next(kStagesA);
+          ra.next(C::kStagesA);
           rb.next(C::kStagesB);
         }
         if (!ok) break;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, cq = lane & 3;
     Ring rr, ra, racc;
     bool ok = true;
-    Tile pend;               // gate/up: the tile whose epilogue share is still due
+    Tile pend = {0, 0, 0, 0};   // gate/up: the tile whose epilogue share is still due
     bool have = false;
     // this warp's third of a gate/up tile's epilogue (warps 0-3 the middle,
     // 4-7 the last third of the 32-column chunks)
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < nks; ++ks) {
         // the A ring is full at this point: the MMA waits for the previous
         // tile's epilogue before it takes stage 0 of this one
-        if (GU && have && ks == kStagesA && !epilogue_share()) {
+        if (GU && have && ks == C::kStagesA && !epilogue_share()) {
           ok = false;
           break;
         }
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&raw_empty[rr.i]);
         }
         rr.next(C::kStagesRaw);
-        ra.next(kStagesA);
+        ra.next(C::kStagesA);
       }
       if (GU && ok) {
         pend = tl;
