@@ -41,8 +41,8 @@ template <bool GU>
 struct Cfg {
   static constexpr int kMats = GU ? 2 : 1;
   static constexpr int kStagesA = 3;             // dequantised FP16 A stages
-  static constexpr int kStagesB = GU ? 3 : 4;
-  static constexpr int kStagesRaw = GU ? 3 : 10;   // int4 chunks (+ scales) from HBM
+  static constexpr int kStagesB = GU ? 3 : 5;
+  static constexpr int kStagesRaw = 3;             // int4 chunks (+ scales) from HBM
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
   static constexpr int kBBytes = kNMax * kBK * 2;         // 32 KB
@@ -206,10 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t va[32], vb[32];
       tmem_ld32(taddr + col0, va);
       if (GU) tmem_ld32(taddr + 256u + col0, vb);
+      // down: the 32 columns' pair indices, one coalesced load, broadcast below
+      const int my_pair = (!GU && col0 + lane < et.n) ? c.sorted[et.r0 + col0 + lane] : 0;
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int nn = col0 + j;
+        const int pair = GU ? 0 : __shfl_sync(0xffffffffu, my_pair, j);
         if (nn < et.n) {
           if (GU) {
             float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
@@ -220,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
           } else {
-            const int pair = c.sorted[et.r0 + nn];
             c.ybuf[(size_t)pair * c.H + et.m0 + row] = __uint_as_float(va[j]);
           }
         }
