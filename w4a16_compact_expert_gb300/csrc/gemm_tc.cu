@@ -206,8 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t va[32], vb[32];
       tmem_ld32(taddr + col0, va);
       if (GU) tmem_ld32(taddr + 256u + col0, vb);
-      // down: the 32 columns' pair indices, one coalesced load, broadcast below
-      const int my_pair = (!GU && col0 + lane < et.n) ? c.sorted[et.r0 + col0 + lane] : 0;
+      // the 32 columns' pair indices (down) or PRENORM row scales (gate/up):
+      // one coalesced load per chunk, broadcast below
+      int my_pair = 0;
+      float my_rn = 1.f;
+      if (col0 + lane < et.n) {
+        if (!GU) my_pair = c.sorted[et.r0 + col0 + lane];
+        else if (c.flags & 2u) my_rn = c.rnorm[c.sorted[et.r0 + col0 + lane] / c.k];
+      }
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (GU) {
             float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
             if (c.flags & 2u) {
-              const float r = c.rnorm[c.sorted[et.r0 + nn] / c.k];
+              const float r = __shfl_sync(0xffffffffu, my_rn, j);
               gv *= r;
               uv *= r;
             }
