@@ -68,9 +68,11 @@ def parse():
     ap.add_argument("--workload", choices=["decode", "prefill", "qwen", "stack"], default="decode")
     ap.add_argument("--variant", type=int, default=1, help="prefill: 1 = no bias, 2 = logit bias ~ N(0, 1)")
     ap.add_argument("--tokens", type=int, default=None, help="T per layer forward")
-    ap.add_argument("--force", choices=["auto", "gemv", "unfused", "gemm"], default="auto",
+    ap.add_argument("--force", choices=["auto", "gemv", "unfused", "gemm", "offload"], default="auto",
                     help="gemv: decode kernels (single launch when it fits); unfused: decode kernels as "
-                         "separate launches; gemm: tensor-core grouped GEMM")
+                         "separate launches; gemm: tensor-core grouped GEMM; offload: the offload-qpacked "
+                         "comparison (expansion into FP16 execution slots, then the dense grouped GEMM)")
+    ap.add_argument("--offload-slots", type=int, default=16, help="FP16 execution slots for --force offload")
     ap.add_argument("--sweep", action="store_true", help="stack: T sweep with both kernel families")
     ap.add_argument("--cache", action="store_true",
                     help="qwen: partial residency through the expert cache (misses copied from host memory)")
@@ -292,6 +294,8 @@ class Workload:
                     self.biases.append(torch.randn(s.E, device=dev, generator=g).float())
                 else:
                     self.biases.append(None)
+            if getattr(args, "force", "auto") == "offload":
+                m.offload_enable(args.offload_slots)
             self.layers.append(m)
         g.manual_seed(20_000)
         if self.chain:
@@ -485,7 +489,8 @@ def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
 
 def force_flag(name):
     from w4a16_compact_expert_gb300 import moe_w4a16 as M
-    return {"auto": 0, "gemv": M.FORCE_GEMV, "unfused": M.FORCE_GEMV | M.UNFUSED, "gemm": M.FORCE_GEMM}[name]
+    return {"auto": 0, "gemv": M.FORCE_GEMV, "unfused": M.FORCE_GEMV | M.UNFUSED, "gemm": M.FORCE_GEMM,
+            "offload": M.OFFLOAD}[name]
 
 
 def gpu_arm(args, rank, world, local_rank):
@@ -528,6 +533,13 @@ def gpu_arm(args, rank, world, local_rank):
         "gpu_launches": steps * wl.L * launches, "launches_per_layer_forward": launches,
         "clocks": clocks, "kernel_src": sha,
     }
+    if path == moe_w4a16.PATH_OFFLOAD:
+        # what the expansion moves per layer, next to the compact path's weight bytes
+        exp_bytes = avg_u * 3 * s.I * s.H * 2
+        res["offload"] = {"execution_slots": args.offload_slots, "avg_active_experts": avg_u,
+                          "expanded_fp16_bytes_written_per_layer": exp_bytes,
+                          "fp16_weight_bytes_read_per_layer": exp_bytes,
+                          "compact_weight_bytes_per_layer": avg_u * s.expert_bytes}
     wl.close()
     return res
 

@@ -90,6 +90,8 @@ typedef enum {
 #define MOE_W4A16_FORCE_GEMM 8u   /* tensor-core grouped GEMM whatever T is */
 #define MOE_W4A16_UNFUSED   16u   /* decode regime as separate route / gate-up / down launches
                                      instead of the single cooperative launch used for T <= 64 */
+#define MOE_W4A16_OFFLOAD   32u   /* the offload-qpacked comparison path (see
+                                     moe_w4a16_offload_enable); excludes FORCE_GEMV */
 
 typedef struct {
   int32_t hidden;       /* H: multiple of 64, >= 64 */
@@ -235,15 +237,35 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h
  *   MOE_W4A16_PATH_DECODE        router (1 or 4 kernels) + gate/up + down
  *   MOE_W4A16_PATH_GEMM          router (1 or 4) + gather + gate/up GEMM +
  *                                down GEMM + combine
+ *   MOE_W4A16_PATH_OFFLOAD       router (1 or 4) + gather + per batch of
+ *                                execution slots (expand + dense gate/up GEMM
+ *                                + dense down GEMM) + combine
  * PATH_NONE before any forward and after one with T == 0.  *launches may be
  * NULL.  Returns -1 for a NULL handle. */
 enum {
   MOE_W4A16_PATH_NONE = 0,
   MOE_W4A16_PATH_DECODE_FUSED = 1,
   MOE_W4A16_PATH_DECODE = 2,
-  MOE_W4A16_PATH_GEMM = 3
+  MOE_W4A16_PATH_GEMM = 3,
+  MOE_W4A16_PATH_OFFLOAD = 4
 };
 MOE_W4A16_API int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches);
+
+/* The offload-qpacked comparison ("Horizon RunMap - architecture",
+ * "Representation and computation" and its profile list: the historical
+ * profile that dequantises a low-bit source into bounded FP16/BF16 execution
+ * slots).  It is the baseline the compact path is measured against, not the
+ * hot path.  Allocates n_slots FP16 execution slots on the handle's device
+ * (each 3 * inter * hidden * 2 bytes: gate, up and down expanded, row-major;
+ * owned by the handle, freed by destroy; a second call replaces them).  A
+ * forward with MOE_W4A16_OFFLOAD then routes as usual, expands each batch of at
+ * most n_slots active experts into the slots and runs the grouped GEMM on the
+ * FP16 copies (w = q * s rounded to the nearest FP16, the same values the
+ * compact GEMM dequantises in shared memory), so its outputs match the compact
+ * GEMM path up to FP32 summation order.
+ * Errors: INVALID_ARG (NULL handle, n_slots outside [1, 64], shapes the
+ * grouped GEMM does not take), CUDA (allocation or tensor-map encoding). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_offload_enable(moe_w4a16_handle* h, int32_t n_slots);
 
 
 /* Failure-detection self-test (the pages have no counterpart).  Enqueues

@@ -247,6 +247,34 @@ moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h, int32_t t_st
   return MOE_W4A16_OK;
 }
 
+moe_w4a16_status moe_w4a16_offload_enable(moe_w4a16_handle* h, int32_t n_slots) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  if (n_slots < 1 || n_slots > 64) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "n_slots outside [1, 64]");
+  if (!gemm_shapes_supported(h->cfg.hidden, h->cfg.inter))
+    return fail(h, MOE_W4A16_ERR_INVALID_ARG, "the grouped GEMM does not take these shapes");
+  DeviceGuard dg(h->cfg.device);
+  if (!dg.ok) return fail(h, MOE_W4A16_ERR_CUDA, "cudaSetDevice failed");
+  if (h->xpool) {   // replace the previous execution slots
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e, "synchronize before freeing the execution slots");
+    for (size_t i = 0; i < h->allocs.size(); ++i)
+      if (h->allocs[i] == h->xpool) {
+        cudaFree(h->allocs[i]);
+        h->allocs.erase(h->allocs.begin() + (long)i);
+        break;
+      }
+    h->xpool = nullptr;
+    h->xslots = 0;
+  }
+  const size_t halves = (size_t)n_slots * 3 * h->cfg.inter * h->cfg.hidden;
+  cudaError_t e = dalloc(h, &h->xpool, halves);
+  if (e != cudaSuccess) return cuda_fail(h, e, "execution slot allocation");
+  h->dmaps = make_dense_maps(h->xpool, h->cfg.hidden, h->cfg.inter, n_slots);
+  if (!h->dmaps.ok) return fail(h, MOE_W4A16_ERR_CUDA, "execution slot tensor maps");
+  h->xslots = n_slots;
+  return MOE_W4A16_OK;
+}
+
 moe_w4a16_status moe_w4a16_pack_experts(moe_w4a16_handle* h, int32_t slot0, int32_t n, const uint8_t* gate_q,
                                         const uint16_t* gate_s, const uint8_t* up_q, const uint16_t* up_s,
                                         const uint8_t* down_q, const uint16_t* down_s, moe_w4a16_stream_t stream) {
@@ -346,6 +374,9 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.xp = h->xp;
   c.hbuf = h->hbuf;
   c.ybuf = h->ybuf;
+  c.xpool = h->xpool;
+  c.xslots = h->xslots;
+  c.xslot_halves = (uint64_t)3 * h->cfg.inter * h->cfg.hidden;
   c.route_hist = h->route_hist;
   c.route_counter = h->counters + route_counter_word(h->cfg.hidden);
   c.grid_bar = reinterpret_cast<unsigned long long*>(h->counters);
@@ -361,9 +392,13 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (!h) return MOE_W4A16_ERR_INVALID_ARG;
   if (T < 0 || T > h->cfg.max_tokens)
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "T=" + std::to_string(T) + " outside [0, max_tokens]");
-  if (flags & ~31u) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "unknown flag bits");
+  if (flags & ~63u) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "unknown flag bits");
   if ((flags & MOE_W4A16_FORCE_GEMV) && (flags & MOE_W4A16_FORCE_GEMM))
     return fail(h, MOE_W4A16_ERR_INVALID_ARG, "FORCE_GEMV and FORCE_GEMM are exclusive");
+  const bool offload = flags & MOE_W4A16_OFFLOAD;
+  if (offload && (flags & MOE_W4A16_FORCE_GEMV))
+    return fail(h, MOE_W4A16_ERR_INVALID_ARG, "OFFLOAD and FORCE_GEMV are exclusive");
+  if (offload && h->xslots < 1) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "OFFLOAD needs moe_w4a16_offload_enable");
   if (T == 0) {
     h->last_path = MOE_W4A16_PATH_NONE;
     h->last_launches = 0;
@@ -387,7 +422,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.bias = bias;
   c.flags = flags;
   c.out = static_cast<__half*>(out);
-  const bool gemm = (flags & MOE_W4A16_FORCE_GEMM) ||
+  const bool gemm = offload || (flags & MOE_W4A16_FORCE_GEMM) ||
                     (!(flags & MOE_W4A16_FORCE_GEMV) && T > h->gemv_max_tokens &&
                      gemm_shapes_supported(h->cfg.hidden, h->cfg.inter));
   const bool fused_route = T <= ROUTE_FUSED_MAX_T;
@@ -399,7 +434,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
   const int route_launches = fused_route && route_single_launch(c) ? 1 : 4;
-  int32_t path = gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
+  int32_t path = offload ? MOE_W4A16_PATH_OFFLOAD : gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
   if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);
   if (e == cudaSuccess) e = record_stage(h->events, 1, st);
@@ -413,7 +448,9 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
       if (e == cudaSuccess) e = launch_gemv_experts(c, st, h->events);
     }
   } else {
-    e = gemm ? launch_gemm_experts(c, h->maps, st, h->events) : launch_gemv_experts(c, st, h->events);
+    e = offload ? launch_offload_experts(c, h->dmaps, st, h->events)
+        : gemm  ? launch_gemm_experts(c, h->maps, st, h->events)
+                : launch_gemv_experts(c, st, h->events);
   }
   if (e == cudaErrorNotSupported) return fail(h, MOE_W4A16_ERR_UNSUPPORTED, "grouped GEMM path not available");
   if (e != cudaSuccess) return cuda_fail(h, e, "expert launch");
@@ -425,7 +462,9 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
     e = cudaMemcpyAsync(expert_offsets, c.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug output copy");
   h->last_path = path;
+  const int batches = offload ? (c.max_active + h->xslots - 1) / h->xslots : 0;
   h->last_launches = path == MOE_W4A16_PATH_DECODE_FUSED ? 1
+                     : path == MOE_W4A16_PATH_OFFLOAD ? route_launches + 2 + 3 * batches
                      : route_launches + (path == MOE_W4A16_PATH_GEMM ? 4 : 2);
   return MOE_W4A16_OK;
 }

@@ -72,7 +72,7 @@ struct Ring {
 };
 
 struct Tile {
-  int slot, r0, n, m0;
+  int slot, r0, n, m0, u;
 };
 
 // The active-expert schedule written by the routing kernels, copied to shared
@@ -83,6 +83,7 @@ struct Sched {
   int* slot;        // [n]
   int* start;       // [n]
   int* count;       // [n]
+  int lo, hi;       // the tiles this launch covers
 };
 
 DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
@@ -118,7 +119,7 @@ DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
 // expert's rows into ceil(count / 256) near-equal parts.
 DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
   if (s.n <= 0) return false;
-  if (t >= s.tile[s.n] * mtiles) return false;
+  if (t >= s.hi) return false;
   const int mt = t % mtiles, ct = t / mtiles;
   int lo = 0, hi = s.n - 1;
   while (lo < hi) {   // last u with tile[u] <= ct
@@ -134,6 +135,7 @@ DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
   out.r0 = s.start[u] + b0;
   out.n = b1 - b0;
   out.m0 = mt * kMTile;
+  out.u = u;
   return true;
 }
 
@@ -141,7 +143,11 @@ DEV_INLINE void st_shared_v2_b32(uint32_t addr, uint32_t v0, uint32_t v1) {
   asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v0), "r"(v1) : "memory");
 }
 
-template <bool GU>
+// DENSE: the offload-qpacked comparison.  A comes as FP16 tiles of the
+// execution slots of the active experts [c.ub0, c.ub1) (tmA0 / tmA1: 3-D maps,
+// 128 rows x 64 K per load, 128-byte swizzled straight into the A ring), no
+// dequantisation; the tile schedule covers only those experts.
+template <bool GU, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(FwdCtx c, const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmS0,
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < C::kStagesA; ++s) {
-      mbar_init(&a_full[s], kDqWarps);
+      mbar_init(&a_full[s], DENSE ? 1 : kDqWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::kStagesB; ++s) {
@@ -187,12 +193,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  const Sched sch = load_sched(c, reinterpret_cast<int*>(smem + C::kOffSched));   // contains __syncthreads
+  Sched sch = load_sched(c, reinterpret_cast<int*>(smem + C::kOffSched));   // contains __syncthreads
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   const MatLayout& LA = GU ? c.lay.gate : c.lay.down;
   const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / kMTile;
+  if (DENSE) {
+    sch.lo = sch.tile[min(c.ub0, sch.n)] * mtiles;
+    sch.hi = sch.tile[min(c.ub1, sch.n)] * mtiles;
+  } else {
+    sch.lo = 0;
+    sch.hi = sch.n > 0 ? sch.tile[sch.n] * mtiles : 0;
+  }
   const int nacc = GU ? 1 : 2;   // accumulator buffers (gate/up uses all 512 columns)
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
   // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32).
@@ -236,11 +249,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (warp == kWarpProd) {
+  if (DENSE && warp == kWarpProd) {
+    // ----------------------------------------- FP16 A producer (comparison)
+    if (lane == 0) {
+      Ring ra;
+      for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
+        Tile tl;
+        if (!get_tile(sch, t, mtiles, tl)) break;
+        bool ok = true;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + C::kOffA + ra.i * C::kABytes;
+          mbar_expect_tx(&a_full[ra.i], (uint32_t)C::kABytes);
+          tma_load_3d(dst, &tmA0, ks * kBK, tl.m0, tl.u - c.ub0, &a_full[ra.i]);
+          if (GU) tma_load_3d(dst + C::kAMat, &tmA1, ks * kBK, tl.m0, tl.u - c.ub0, &a_full[ra.i]);
+          ra.next(C::kStagesA);
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpProd) {
     // ------------------------------------------------- int4 chunk producer
     if (lane == 0) {
       Ring rr;
-      for (int t = blockIdx.x;; t += gridDim.x) {
+      for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
         if (!get_tile(sch, t, mtiles, tl)) break;
         bool ok = true;
@@ -268,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- token tile producer
     if (lane == 0) {
       Ring rb;
-      for (int t = blockIdx.x;; t += gridDim.x) {
+      for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
         if (!get_tile(sch, t, mtiles, tl)) break;
         const int nq = (tl.n + 63) / 64;
@@ -292,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       Ring ra, rb, racc;
       bool ok = true;
-      for (int t = blockIdx.x; ok; t += gridDim.x) {
+      for (int t = sch.lo + blockIdx.x; ok; t += gridDim.x) {
         Tile tl;
         if (!get_tile(sch, t, mtiles, tl)) break;
         const int n16 = (tl.n + 15) & ~15;
@@ -348,7 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       have = false;
       return true;
     };
-    for (int t = blockIdx.x; ok; t += gridDim.x) {
+    if (DENSE) {   // no dequantisation: the gate/up epilogue shares only
+      for (int t = sch.lo + blockIdx.x; GU; t += gridDim.x) {
+        if (!get_tile(sch, t, mtiles, pend) || !epilogue_share()) break;
+      }
+    }
+    for (int t = sch.lo + blockIdx.x; ok && !DENSE; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, tl)) break;
       // the scales of the thread's rows for the current block (read from the
@@ -421,12 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         have = true;
       }
     }
-    if (GU && ok && have) epilogue_share();   // the last tile
+    if (GU && !DENSE && ok && have) epilogue_share();   // the last tile
   } else {
     // ----------------------------------------------------------- epilogue
     // warps 8..11 -> TMEM lane quarters 0..3
     Ring racc;
-    for (int t = blockIdx.x;; t += gridDim.x) {
+    for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, tl)) break;
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) break;
@@ -603,21 +644,82 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
   CUtensorMap mx, mh;
   if (!make_map(&mx, c.xp, P, (uint64_t)c.H, 64) || !make_map(&mh, c.hbuf, P, (uint64_t)c.I, 64))
     return cudaErrorNotSupported;
-  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true>, Cfg<true>::kSmem);
-  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false>, Cfg<false>::kSmem);
+  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, false>, Cfg<true>::kSmem);
+  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, false>, Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = c.num_sms > 0 ? c.num_sms : 148;
   e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess)
-    e = launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
+    e = launch_pdl(grouped_gemm_kernel<true, false>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
                    pm.q[1], pm.sc[0], pm.sc[1]);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess)
-    e = launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh, pm.q[2],
+    e = launch_pdl(grouped_gemm_kernel<false, false>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh, pm.q[2],
                    pm.q[2], pm.sc[2], pm.sc[2]);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c);
+  if (e == cudaSuccess) e = record_stage(se, 4, st);
+  return e;
+}
+
+DenseMaps make_dense_maps(const __half* xpool, int H, int I, int xslots) {
+  DenseMaps dm;
+  memset(&dm, 0, sizeof dm);
+  dm.ok = false;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !xpool || xslots < 1 || !gemm_shapes_supported(H, I)) return dm;
+  const uint64_t slot_bytes = (uint64_t)3 * I * H * 2;
+  // gate and up: [slot][I][H]; down: [slot][H][I]; 128 rows x 64 K per box, 128-byte swizzle
+  const uint64_t off[3] = {0, (uint64_t)I * H, (uint64_t)2 * I * H};
+  const uint64_t rows[3] = {(uint64_t)I, (uint64_t)I, (uint64_t)H}, ks[3] = {(uint64_t)H, (uint64_t)H, (uint64_t)I};
+  for (int m = 0; m < 3; ++m) {
+    const cuuint64_t dims[3] = {ks[m], rows[m], (cuuint64_t)xslots};
+    const cuuint64_t strides[2] = {ks[m] * 2, slot_bytes};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kMTile, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&dm.a[m], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(xpool + off[m]), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return dm;
+  }
+  dm.ok = true;
+  return dm;
+}
+
+// The offload-qpacked comparison: the routed x rows gathered once, then per
+// batch of at most xslots active experts an expansion into the FP16 execution
+// slots and the dense gate/up and down grouped GEMMs, then the combine.  The
+// number of batches is bounded by max_active on the host; a batch past the
+// active experts exits on the device.
+cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, cudaStream_t st, const StageEvents& se) {
+  if (!gemm_shapes_supported(c0.H, c0.I) || !dm.ok || c0.xslots < 1) return cudaErrorNotSupported;
+  const uint64_t P = (uint64_t)c0.T * c0.k;
+  CUtensorMap mx, mh;
+  if (!make_map(&mx, c0.xp, P, (uint64_t)c0.H, 64) || !make_map(&mh, c0.hbuf, P, (uint64_t)c0.I, 64))
+    return cudaErrorNotSupported;
+  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, true>, Cfg<true>::kSmem);
+  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, true>, Cfg<false>::kSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = c0.num_sms > 0 ? c0.num_sms : 148;
+  e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c0);
+  const int nb = (c0.max_active + c0.xslots - 1) / c0.xslots;
+  for (int b = 0; b < nb && e == cudaSuccess; ++b) {
+    FwdCtx c = c0;
+    c.ub0 = b * c0.xslots;
+    c.ub1 = c.ub0 + c0.xslots < c0.max_active ? c.ub0 + c0.xslots : c0.max_active;
+    e = launch_expand(c, st);
+    if (e == cudaSuccess)
+      e = launch_pdl(grouped_gemm_kernel<true, true>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx,
+                     dm.a[0], dm.a[1], dm.a[0], dm.a[1]);
+    if (e == cudaSuccess)
+      e = launch_pdl(grouped_gemm_kernel<false, true>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh,
+                     dm.a[2], dm.a[2], dm.a[2], dm.a[2]);
+  }
+  if (e == cudaSuccess) e = record_stage(se, 2, st);
+  if (e == cudaSuccess) e = record_stage(se, 3, st);
+  if (e == cudaSuccess)
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c0.T * ((c0.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c0);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }

@@ -37,6 +37,9 @@ struct moe_w4a16_handle {
   __half* xp = nullptr;
   __half* hbuf = nullptr;
   float* ybuf = nullptr;
+  __half* xpool = nullptr;           // offload-qpacked comparison: FP16 execution slots
+  int xslots = 0;
+  DenseMaps dmaps{};
   unsigned* counters = nullptr;      // counter_words(H): grid barrier, arrival and readiness counters
   DevStatus* status = nullptr;
   uint8_t* stage = nullptr;          // pack staging for host sources

@@ -52,6 +52,11 @@ struct FwdCtx {
   DevStatus* status;
   int num_sms;
   int max_active;              // upper bound of active experts: min(E, T*k)
+  // offload-qpacked comparison path: FP16 execution slots
+  __half* xpool;               // [xslots][gate I*H | up I*H | down H*I], row-major, K contiguous
+  uint64_t xslot_halves;       // halves per execution slot (3 I H)
+  int xslots;                  // execution slots
+  int ub0, ub1;                // the active experts [ub0, ub1) expanded into slots 0 .. ub1 - ub0 - 1
 };
 
 // Device counter block of a handle, in 32-bit words: [0, 2) the 64-bit grid
@@ -105,6 +110,17 @@ struct PoolMaps {
 };
 PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slots);
 cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_t st, const StageEvents& se);
+
+// The offload-qpacked comparison path: each batch of at most xslots active
+// experts is expanded into FP16 execution slots (offload.cu), then the same
+// grouped GEMM runs with dense FP16 A tiles loaded by TMA (gemm_tc.cu).
+struct DenseMaps {
+  CUtensorMap a[3];   // gate, up, down of the execution slots: [slot][rows][K] FP16, boxes of 128 rows x 64 K
+  bool ok;
+};
+DenseMaps make_dense_maps(const __half* xpool, int H, int I, int xslots);
+cudaError_t launch_expand(const FwdCtx& c, cudaStream_t st);   // active experts [c.ub0, c.ub1)
+cudaError_t launch_offload_experts(const FwdCtx& c, const DenseMaps& dm, cudaStream_t st, const StageEvents& se);
 
 // route: the largest T handled by the single-launch cluster router
 #define ROUTE_FUSED_MAX_T 64

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_w4a16.so")
 OK, ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_PACKED, ERR_NOT_RESIDENT, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
 STATUS_NAMES = ["OK", "ERR_INVALID_ARG", "ERR_CUDA", "ERR_OOM", "ERR_NOT_PACKED", "ERR_NOT_RESIDENT",
                 "ERR_TIMEOUT", "ERR_UNSUPPORTED"]
-RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED = 1, 2, 4, 8, 16
+RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED, OFFLOAD = 1, 2, 4, 8, 16, 32
 
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
             "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
@@ -27,9 +27,10 @@ EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "
             "moe_w4a16_cache_create", "moe_w4a16_cache_destroy", "moe_w4a16_cache_acquire",
             "moe_w4a16_cache_release", "moe_w4a16_cache_get_stats", "moe_w4a16_cache_slot_of",
             "moe_w4a16_cache_last_error", "moe_w4a16_cache_create_sim", "moe_w4a16_cache_sim_complete",
-            "moe_w4a16_cache_sim_fail", "moe_w4a16_selftest_timeout"]
-PATH_NONE, PATH_DECODE_FUSED, PATH_DECODE, PATH_GEMM = 0, 1, 2, 3
-PATH_NAMES = {PATH_NONE: "none", PATH_DECODE_FUSED: "decode_fused", PATH_DECODE: "decode", PATH_GEMM: "gemm"}
+            "moe_w4a16_cache_sim_fail", "moe_w4a16_selftest_timeout", "moe_w4a16_offload_enable"]
+PATH_NONE, PATH_DECODE_FUSED, PATH_DECODE, PATH_GEMM, PATH_OFFLOAD = 0, 1, 2, 3, 4
+PATH_NAMES = {PATH_NONE: "none", PATH_DECODE_FUSED: "decode_fused", PATH_DECODE: "decode", PATH_GEMM: "gemm",
+              PATH_OFFLOAD: "offload_qpacked"}
 
 
 class Config(ctypes.Structure):
@@ -86,6 +87,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_get_gemv_max_tokens.restype = i32
     lib.moe_w4a16_set_gemv_max_tokens.argtypes = [vp, i32]
     lib.moe_w4a16_set_stage_events.argtypes = [vp, vp]
+    lib.moe_w4a16_offload_enable.argtypes = [vp, i32]
     lib.moe_w4a16_last_path.argtypes = [vp, ctypes.POINTER(i32)]
     lib.moe_w4a16_last_path.restype = i32
     u64, u64p = ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)
@@ -171,6 +173,10 @@ class MoELayer:
     @gemv_max_tokens.setter
     def gemv_max_tokens(self, v: int):
         self._check(self.lib.moe_w4a16_set_gemv_max_tokens(self.h, int(v)))
+
+    def offload_enable(self, n_slots: int):
+        """FP16 execution slots for the offload-qpacked comparison path (forward flag OFFLOAD)."""
+        self._check(self.lib.moe_w4a16_offload_enable(self.h, int(n_slots)))
 
     def last_path(self):
         """(path, kernel launches) of the last forward: PATH_* and a count."""
