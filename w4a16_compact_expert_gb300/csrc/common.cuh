@@ -254,15 +254,6 @@ DEV_INLINE void tma_load_2d(void* dst, const void* tmap, int c0, int r0, uint64_
       : "memory");
 }
 
-// TMA: one box at (c0, c1, c2) of a 3-D tensor map.
-DEV_INLINE void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA: one box at (c0, c1, c2, c3) of a 4-D tensor map (no swizzle).
 DEV_INLINE void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, uint64_t* bar) {
   asm volatile(

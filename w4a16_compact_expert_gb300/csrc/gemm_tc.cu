@@ -139,6 +139,15 @@ DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
   return true;
 }
 
+// TMA: one box at (c0, c1, c2) of a 3-D tensor map.
+DEV_INLINE void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 DEV_INLINE void st_shared_v2_b32(uint32_t addr, uint32_t v0, uint32_t v1) {
   asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v0), "r"(v1) : "memory");
 }
