@@ -81,6 +81,7 @@ def parse():
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-max-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-warmup", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -143,6 +144,9 @@ def cpu_leg(args):
     flags = (moe_oracle.FLAG_RESIDUAL | moe_oracle.FLAG_PRENORM) if args.workload == "stack" else 0
     xs = [synth.draw_x(seed + r, T, layer.shape.hidden) for r in range(ROTATE)]
     experts = layer.slot_experts().arrays()
+    for w in range(args.cpu_warmup):   # untimed
+        moe_oracle.moe_layer(xs[w % ROTATE], layer.router_w, layer.bias, experts, layer.shape.top_k, flags,
+                             layer.expert_to_slot)
     done, t0 = 0, time.perf_counter()
     while True:
         moe_oracle.moe_layer(xs[done % ROTATE], layer.router_w, layer.bias, experts, layer.shape.top_k, flags,
@@ -154,11 +158,11 @@ def cpu_leg(args):
     print(json.dumps({"value": T * done / el, "steps": done, "seconds": el, "tokens": T}))
 
 
-def run_cpu_leg(args, seconds, max_steps=0):
+def run_cpu_leg(args, seconds, max_steps=0, warmup=0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-leg", "--workload", args.workload,
            "--variant", str(args.variant), "--tokens", str(tokens_of(args)), "--cpu-seconds", str(seconds),
-           "--cpu-max-steps", str(max_steps)]
+           "--cpu-max-steps", str(max_steps), "--cpu-warmup", str(warmup)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 4 + 300)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
@@ -666,9 +670,9 @@ def main():
         if rank != 0:
             return
         steps = args.steps or 20
-        leg = run_cpu_leg(args, seconds=150.0, max_steps=steps + args.warmup)
+        leg = run_cpu_leg(args, seconds=150.0, max_steps=steps, warmup=args.warmup)
         res = {"impl": "reference", "metric": METRIC, "value": leg["value"], "unit": UNIT, "n_gpus": args.gpus,
-               "steps": leg["steps"], "warmup": 0, "ms_per_step": leg["seconds"] * 1e3 / leg["steps"],
+               "steps": leg["steps"], "warmup": args.warmup, "ms_per_step": leg["seconds"] * 1e3 / leg["steps"],
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                "data": "synthetic (seeded)", "config": workload_config(args, T),
                "cpu_baseline": {"value": leg["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
