@@ -457,7 +457,7 @@ def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
                 "gemv_down_kernel": (stage_avg[2] + stage_avg[3], stage_bytes[2], 2.0 * P * s.H * s.I)}
         srcs = ["gemv.cu", "gemv_dev.cuh", "common.cuh", "layout.h"]
     else:
-        kern = {"route": (stage_avg[0], stage_bytes[0], 2.0 * T * s.E * s.H),
+        kern = {"route + gather_rows": (stage_avg[0], stage_bytes[0], 2.0 * T * s.E * s.H),
                 "grouped_gemm_kernel<gate_up>": (stage_avg[1], stage_bytes[1], 2.0 * P * 2 * s.H * s.I),
                 "grouped_gemm_kernel<down>": (stage_avg[2], stage_bytes[2], 2.0 * P * s.H * s.I),
                 "combine_kernel": (stage_avg[3], 0, 0.0)}

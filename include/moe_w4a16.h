@@ -213,8 +213,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_route_noalloc(const void* x, int32_t T,
 /* Profiling aid.  With events != NULL (an array of 5 cudaEvent_t created by
  * the caller with timing enabled), every later forward on this handle records
  * them on its stream at the stage boundaries: [0] before routing, [1] after
- * routing, [2] after the gate/up kernel, [3] after the down kernel, [4] after
- * the combine ([4] == [3] on the separate-launch decode path, whose down
+ * routing (on the grouped-GEMM path: after the gather of the x rows that
+ * follows routing), [2] after the gate/up kernel, [3] after the down kernel,
+ * [4] after the combine ([4] == [3] on the separate-launch decode path, whose down
  * kernel also does the combine; on the single-launch decode path [1] == [0]
  * and [2] == [3] == [4] bracket the one fused kernel).  While the stream is
  * being captured they are recorded as external event nodes of the graph.

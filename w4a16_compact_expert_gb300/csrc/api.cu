@@ -437,7 +437,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   int32_t path = offload ? MOE_W4A16_PATH_OFFLOAD : gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
   if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);
-  if (e == cudaSuccess) e = record_stage(h->events, 1, st);
+  if (e == cudaSuccess && !gemm) e = record_stage(h->events, 1, st);   // the GEMM family records it after the gather
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   if (fused) {
     e = launch_fused_decode(c, st, h->events);

@@ -5,8 +5,9 @@
 // design is not published).
 //
 // Grid = one CTA per SM, all co-resident (cooperative launch).  A CTA has 12
-// compute warps in NG groups of GW (6 x 2 for T <= 2, 3 x 4 for T <= 8, 2 x 6
-// above), one producer warp and one signaller warp.
+// compute warps in NG groups of GW (6 x 2 for one token routed to >= 8
+// experts, 3 x 4 for T <= 8, 2 x 6 above), one producer warp and one signaller
+// warp.
 //   routing  the grid's warps take the (token, expert, K half) dot products
 //            of the router (and per-token sums of squares for PRENORM) ->
 //            global; one bounded grid barrier; then every CTA reads the logits
@@ -58,9 +59,10 @@ constexpr int kMaxExperts = 256;               // readiness counters per handle
 constexpr uint32_t kSmemBudget = 226 * 1024;
 
 // warps per compute group for a batch of T tokens
-// (2-warp groups give the most items in flight for one or two tokens; from 3
-// tokens on, fewer and wider groups spend less on the cross-warp reductions)
-__host__ __device__ inline int fused_group_warps(int T) { return T <= 2 ? 2 : T <= 8 ? 4 : 6; }
+// (measured: 2-warp groups, the most items in flight, help only one token
+// routed to 8 or more experts; otherwise fewer and wider groups spend less on
+// the cross-warp reductions)
+__host__ __device__ inline int fused_group_warps(int T, int k) { return T == 1 && k >= 8 ? 2 : T <= 8 ? 4 : 6; }
 
 struct FusedSmem {
   uint32_t ns, slot_bytes, off_x, off_h, off_red, off_sb, off_route, total;
@@ -927,13 +929,13 @@ cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
 // kMinSlots weight entries.
 bool fused_decode_supported(const FwdCtx& c, int max_smem) {
   if (c.T > kMaxT || c.T * c.k > kMaxP || c.H % 64 || c.I % 64 || c.k > 32 || c.E > kMaxExperts) return false;
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T));
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T, c.k));
   return L.ns >= (uint32_t)kMinSlots && L.total <= kSmemBudget && (int)L.total <= max_smem;
 }
 
 cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
-  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T));
-  const int gw = fused_group_warps(c.T);
+  const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T, c.k));
+  const int gw = fused_group_warps(c.T, c.k);
   cudaError_t e = gw == 2 ? launch_fused<2>(c, L, st) : gw == 4 ? launch_fused<4>(c, L, st) : launch_fused<6>(c, L, st);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);

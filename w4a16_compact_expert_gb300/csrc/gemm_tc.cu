@@ -658,6 +658,7 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
   if (e != cudaSuccess) return e;
   const int grid = c.num_sms > 0 ? c.num_sms : 148;
   e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
+  if (e == cudaSuccess) e = record_stage(se, 1, st);
   if (e == cudaSuccess)
     e = launch_pdl(grouped_gemm_kernel<true, false>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
                    pm.q[1], pm.sc[0], pm.sc[1]);
@@ -712,6 +713,7 @@ cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, cudaSt
   if (e != cudaSuccess) return e;
   const int grid = c0.num_sms > 0 ? c0.num_sms : 148;
   e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c0);
+  if (e == cudaSuccess) e = record_stage(se, 1, st);
   const int nb = (c0.max_active + c0.xslots - 1) / c0.xslots;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
     FwdCtx c = c0;
