@@ -1,21 +1,26 @@
 // Prefill regime: persistent grouped GEMM on the 5th-generation tensor cores
 // (tcgen05.mma, FP16 operands in shared memory, FP32 accumulators in TMEM).
 //
-// The compact int4 weights are the MMA A operand (M = 128 weight rows per
-// tile); the tokens of one expert are the N dimension (N <= 256, padded only
-// to a multiple of 16, so ragged expert loads waste little work).  Per 64-wide
-// K step:
-//   producer warp : one 4-D TMA load fetches the int4 chunks of the 8 row
-//                   tiles of a matrix into a raw ring; the token rows of B come
-//                   as 2-D TMA tiles, 128-byte swizzled (x gathered into
-//                   sorted-row order by a small kernel for gate/up; h for down)
+// The compact int4 weights are the MMA A operand: two 128-row A matrices per
+// tile share every token stage (gate/up: the gate and up rows m0 .. m0 + 127;
+// down: rows m0 .. m0 + 255 of the down matrix as two halves).  The tokens of
+// one expert are the N dimension (a token chunk of <= 256, padded only to a
+// multiple of 16, so ragged expert loads waste little work).  Per 64-wide K
+// step:
+//   producer warp : 4-D TMA loads fetch the int4 chunks of the 8 row tiles of
+//                   each A matrix (and, at scale-block starts, their block
+//                   scales) into a raw ring; the token rows of B come as 2-D
+//                   TMA tiles, 128-byte swizzled (x gathered into sorted-row
+//                   order by a small kernel for gate/up; h for down)
 //   dequant warps : int4 -> FP16 (nearest q*s) written into a 128-byte
 //                   swizzled K-major A ring (the only place an expanded value
-//                   exists: one 64-wide K step of 128 rows, per CTA)
-//   MMA warp      : one thread issues tcgen05.mma M128 x N x K16 (gate and up
-//                   into two accumulators) and commits stage releases
-//   epilogue warps: tcgen05.ld of the accumulators; gate/up: h = SiLU(g) * u
-//                   rounded to FP16; down: y [pair][H] FP32
+//                   exists: one 64-wide K step of 2 x 128 rows, per CTA)
+//   MMA warp      : one thread issues tcgen05.mma M128 x N x K16 for each A
+//                   matrix into the two 256-column halves of one TMEM
+//                   accumulator and commits stage releases
+//   epilogue      : tcgen05.ld of the accumulator; gate/up: h = SiLU(g) * u
+//                   rounded to FP16; down: y [pair][H] FP32.  Split over the 4
+//                   epilogue warps and the 8 dequant warps, a third each
 // A last kernel gathers out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order.
 // Every wait is bounded (status word + early exit), nothing spins forever.
 // Sources: compact weights converted in-kernel with FP32 accumulation stages
@@ -39,9 +44,11 @@ constexpr uint32_t kTmemCols = 512;
 
 template <bool GU>
 struct Cfg {
-  static constexpr int kMats = GU ? 2 : 1;
+  // two 128-row A tiles share every token stage: gate and up (gate/up), rows
+  // m0 and m0 + 128 of the down matrix (down)
+  static constexpr int kMats = 2;
   static constexpr int kStagesA = 3;             // dequantised FP16 A stages
-  static constexpr int kStagesB = GU ? 3 : 5;
+  static constexpr int kStagesB = 3;
   static constexpr int kStagesRaw = 3;             // int4 chunks (+ scales) from HBM
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
@@ -117,7 +124,7 @@ DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
 
 // Tile t -> (active expert, token chunk, weight-row tile).  Chunks split an
 // expert's rows into ceil(count / 256) near-equal parts.
-DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
+DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, int mstep, Tile& out) {
   if (s.n <= 0) return false;
   if (t >= s.hi) return false;
   const int mt = t % mtiles, ct = t / mtiles;
@@ -134,7 +141,7 @@ DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, Tile& out) {
   out.slot = s.slot[u];
   out.r0 = s.start[u] + b0;
   out.n = b1 - b0;
-  out.m0 = mt * kMTile;
+  out.m0 = mt * mstep;
   out.u = u;
   return true;
 }
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], GU ? 12 : 4);   // one arrive per warp that reads the accumulator
+      mbar_init(&acc_empty[s], 12);   // one arrive per warp that reads the accumulator
     }
     fence_mbar_init();
   }
@@ -207,7 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const MatLayout& LA = GU ? c.lay.gate : c.lay.down;
-  const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / kMTile;
+  // gate/up: tiles of 128 rows of gate and up; down: tiles of 256 rows, the
+  // second 128 rows as the second A matrix (row offset m1off)
+  const int mstep = GU ? kMTile : 2 * kMTile, m1off = GU ? 0 : kMTile;
+  const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / mstep;
   if (DENSE) {
     sch.lo = sch.tile[min(c.ub0, sch.n)] * mtiles;
     sch.hi = sch.tile[min(c.ub1, sch.n)] * mtiles;
@@ -215,19 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     sch.lo = 0;
     sch.hi = sch.n > 0 ? sch.tile[sch.n] * mtiles : 0;
   }
-  const int nacc = GU ? 1 : 2;   // accumulator buffers (gate/up uses all 512 columns)
+  const int nacc = 1;   // one accumulator: the two A matrices' halves fill the 512 columns
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
-  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32).
-  // Gate/up keeps a single accumulator, so its epilogue is on the MMA's
-  // critical path: it is split over the 4 epilogue warps and the 8 dequant
-  // warps (which wait for the MMA at that point anyway), a third each.
-  auto epilogue_chunks = [&](const Tile& et, uint32_t acc_col, int ch0, int ch1) {
+  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32) of
+  // rows m0 + row (first accumulator half) and m0 + 128 + row (second).  The
+  // single accumulator puts the epilogue on the MMA's critical path: it is
+  // split over the 4 epilogue warps and the 8 dequant warps (which wait for the
+  // MMA at that point anyway), a third each.
+  auto epilogue_chunks = [&](const Tile& et, int ch0, int ch1) {
     const int qw = warp & 3, row = qw * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16) + acc_col;
+    const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16);
     for (int col0 = ch0 * 32; col0 < ch1 * 32 && col0 < et.n; col0 += 32) {
-      uint32_t va[32], vb[32];
-      tmem_ld32(taddr + col0, va);
-      if (GU) tmem_ld32(taddr + 256u + col0, vb);
       // the 32 columns' pair indices (down) or PRENORM row scales (gate/up):
       // one coalesced load per chunk, broadcast below
       int my_pair = 0;
@@ -236,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!GU) my_pair = c.sorted[et.r0 + col0 + lane];
         else if (c.flags & 2u) my_rn = c.rnorm[c.sorted[et.r0 + col0 + lane] / c.k];
       }
+      uint32_t va[32], vb[32];
+      tmem_ld32(taddr + col0, va);
+      tmem_ld32(taddr + 256u + col0, vb);
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -251,7 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
           } else {
-            c.ybuf[(size_t)pair * c.H + et.m0 + row] = __uint_as_float(va[j]);
+            float* yr = c.ybuf + (size_t)pair * c.H + et.m0 + row;
+            yr[0] = __uint_as_float(va[j]);
+            yr[kMTile] = __uint_as_float(vb[j]);
           }
         }
       }
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Ring ra;
       for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(sch, t, mtiles, tl)) break;
+        if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         bool ok = true;
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
@@ -274,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = smem + C::kOffA + ra.i * C::kABytes;
           mbar_expect_tx(&a_full[ra.i], (uint32_t)C::kABytes);
           tma_load_3d(dst, &tmA0, ks * kBK, tl.m0, tl.u - c.ub0, &a_full[ra.i]);
-          if (GU) tma_load_3d(dst + C::kAMat, &tmA1, ks * kBK, tl.m0, tl.u - c.ub0, &a_full[ra.i]);
+          tma_load_3d(dst + C::kAMat, &tmA1, ks * kBK, tl.m0 + m1off, tl.u - c.ub0, &a_full[ra.i]);
           ra.next(C::kStagesA);
         }
         if (!ok) break;
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Ring rr;
       for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(sch, t, mtiles, tl)) break;
+        if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         bool ok = true;
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&raw_empty[rr.i], rr.ph ^ 1u, c.status)) {
@@ -298,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool blk = (ks & 3) == 0;   // first K step of a scale block: its scales come along
           mbar_expect_tx(&raw_full[rr.i], blk ? (uint32_t)C::kRawBytes : (uint32_t)C::kRawQ);
           tma_load_4d(dst, &tmA0, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
-          if (GU) tma_load_4d(dst + 8 * 512, &tmA1, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+          tma_load_4d(dst + 8 * 512, &tmA1, 0, ks, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
           if (blk) {
             tma_load_4d(dst + C::kRawQ, &tmS0, 0, ks >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
-            if (GU) tma_load_4d(dst + C::kRawQ + 256, &tmS1, 0, ks >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+            tma_load_4d(dst + C::kRawQ + 256, &tmS1, 0, ks >> 2, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
           }
           rr.next(C::kStagesRaw);
         }
@@ -315,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Ring rb;
       for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(sch, t, mtiles, tl)) break;
+        if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         const int nq = (tl.n + 63) / 64;
         bool ok = true;
         for (int ks = 0; ks < nks; ++ks) {
@@ -339,12 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = sch.lo + blockIdx.x; ok; t += gridDim.x) {
         Tile tl;
-        if (!get_tile(sch, t, mtiles, tl)) break;
+        if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         const int n16 = (tl.n + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kMTile, n16);
         if (!mbar_wait_bounded(&acc_empty[racc.i], racc.ph ^ 1u, c.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (GU ? 0u : (uint32_t)racc.i * 256u);
+        const uint32_t d0 = tmem;
         for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&a_full[ra.i], ra.ph, c.status) ||
               !mbar_wait_bounded(&b_full[rb.i], rb.ph, c.status)) {
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
             const uint32_t acc = (ks | k16) != 0;
             umma_f16_ss(d0, sw128_desc(a_base + k16 * 32), bdesc, idesc, acc);
-            if (GU) umma_f16_ss(tmem + 256u, sw128_desc(a_base + C::kAMat + k16 * 32), bdesc, idesc, acc);
+            umma_f16_ss(tmem + 256u, sw128_desc(a_base + C::kAMat + k16 * 32), bdesc, idesc, acc);
           }
           umma_commit(&a_empty[ra.i]);
           umma_commit(&b_empty[rb.i]);
@@ -385,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) return false;
       tc_fence_after();
       const int nch = (pend.n + 31) / 32, part = 1 + (warp >> 2);
-      epilogue_chunks(pend, 0u, part * nch / 3, (part + 1) * nch / 3);
+      epilogue_chunks(pend, part * nch / 3, (part + 1) * nch / 3);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
@@ -394,20 +407,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     if (DENSE) {   // no dequantisation: the gate/up epilogue shares only
-      for (int t = sch.lo + blockIdx.x; GU; t += gridDim.x) {
-        if (!get_tile(sch, t, mtiles, pend) || !epilogue_share()) break;
+      for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
+        if (!get_tile(sch, t, mtiles, mstep, pend) || !epilogue_share()) break;
       }
     }
     for (int t = sch.lo + blockIdx.x; ok && !DENSE; t += gridDim.x) {
       Tile tl;
-      if (!get_tile(sch, t, mtiles, tl)) break;
+      if (!get_tile(sch, t, mtiles, mstep, tl)) break;
       // the scales of the thread's rows for the current block (read from the
       // raw stage that starts the block)
       __half2 slo[2][1], shi[2][1];
       for (int ks = 0; ks < nks; ++ks) {
         // the A ring is full at this point: the MMA waits for the previous
         // tile's epilogue before it takes stage 0 of this one
-        if (GU && have && ks == C::kStagesA && !epilogue_share()) {
+        if (have && ks == C::kStagesA && !epilogue_share()) {
           ok = false;
           break;
         }
@@ -466,23 +479,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         rr.next(C::kStagesRaw);
         ra.next(C::kStagesA);
       }
-      if (GU && ok) {
+      if (ok) {
         pend = tl;
         have = true;
       }
     }
-    if (GU && !DENSE && ok && have) epilogue_share();   // the last tile
+    if (!DENSE && ok && have) epilogue_share();   // the last tile
   } else {
     // ----------------------------------------------------------- epilogue
     // warps 8..11 -> TMEM lane quarters 0..3
     Ring racc;
     for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
       Tile tl;
-      if (!get_tile(sch, t, mtiles, tl)) break;
+      if (!get_tile(sch, t, mtiles, mstep, tl)) break;
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) break;
       tc_fence_after();
       const int nch = (tl.n + 31) / 32;
-      epilogue_chunks(tl, GU ? 0u : (uint32_t)racc.i * 256u, 0, GU ? nch / 3 : nch);
+      epilogue_chunks(tl, 0, nch / 3);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
@@ -614,7 +627,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 }  // namespace
 
-bool gemm_shapes_supported(int H, int I) { return H % kMTile == 0 && I % kMTile == 0; }
+bool gemm_shapes_supported(int H, int I) { return H % (2 * kMTile) == 0 && I % kMTile == 0; }
 
 PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slots) {
   PoolMaps pm;
