@@ -236,9 +236,10 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h
  *   MOE_W4A16_PATH_DECODE_FUSED  1 cooperative kernel (routing, permutation,
  *                                gate/up, down and combine in one launch)
  *   MOE_W4A16_PATH_DECODE        router (1 or 4 kernels) + gate/up + down
- *   MOE_W4A16_PATH_GEMM          router (1 or 4) + gather + gate/up GEMM +
- *                                down GEMM + combine
- *   MOE_W4A16_PATH_OFFLOAD       router (1 or 4) + gather + per batch of
+ *   MOE_W4A16_PATH_GEMM          router + gather (T <= 64: 1 + 1; above: 2
+ *                                kernels that also gather the x rows) +
+ *                                gate/up GEMM + down GEMM + combine
+ *   MOE_W4A16_PATH_OFFLOAD       router + gather (as above) + per batch of
  *                                execution slots (expand + dense gate/up GEMM
  *                                + dense down GEMM) + combine
  * PATH_NONE before any forward and after one with T == 0.  *launches may be

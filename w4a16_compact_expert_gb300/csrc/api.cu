@@ -182,7 +182,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   ALLOC(h->sorted, P);
   ALLOC(h->p2r, P);
   ALLOC(h->act, 5 * E + 2 + 1);
-  ALLOC(h->route_hist, (size_t)((T + 7) / 8) * E);
+  ALLOC(h->route_hist, (size_t)((T + 7) / 8 + 1) * E);   // + a row of expert totals (cooperative router)
   ALLOC(h->xp, P * H);
   ALLOC(h->hbuf, P * I);
   ALLOC(h->ybuf, P * H);
@@ -379,6 +379,7 @@ static void fill_ctx(moe_w4a16_handle* h, FwdCtx& c) {
   c.xslot_halves = (uint64_t)3 * h->cfg.inter * h->cfg.hidden;
   c.route_hist = h->route_hist;
   c.route_counter = h->counters + route_counter_word(h->cfg.hidden);
+  c.route_bar = reinterpret_cast<unsigned long long*>(h->counters + route_bar_word(h->cfg.hidden));
   c.grid_bar = reinterpret_cast<unsigned long long*>(h->counters);
   c.down_counters = h->counters + 2;
   c.expert_ready = h->counters + 2 + h->cfg.hidden / 32;
@@ -433,10 +434,14 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
-  const int route_launches = fused_route && route_single_launch(c) ? 1 : 4;
+  const bool single_route = fused_route && route_single_launch(c);
+  // the grouped-GEMM family above the single-launch router: logits + one
+  // cooperative kernel that also copies the x rows into sorted-row order
+  const bool route_gathers = gemm && !single_route;
+  const int route_launches = single_route ? 1 : route_gathers ? 2 : 4;
   int32_t path = offload ? MOE_W4A16_PATH_OFFLOAD : gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
-  if (e == cudaSuccess && !fused) e = launch_route(c, fused_route, st);
+  if (e == cudaSuccess && !fused) e = route_gathers ? launch_route_gather(c, st) : launch_route(c, fused_route, st);
   if (e == cudaSuccess && !gemm) e = record_stage(h->events, 1, st);   // the GEMM family records it after the gather
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   if (fused) {
@@ -448,8 +453,8 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
       if (e == cudaSuccess) e = launch_gemv_experts(c, st, h->events);
     }
   } else {
-    e = offload ? launch_offload_experts(c, h->dmaps, st, h->events)
-        : gemm  ? launch_gemm_experts(c, h->maps, st, h->events)
+    e = offload ? launch_offload_experts(c, h->dmaps, route_gathers, st, h->events)
+        : gemm  ? launch_gemm_experts(c, h->maps, route_gathers, st, h->events)
                 : launch_gemv_experts(c, st, h->events);
   }
   if (e == cudaErrorNotSupported) return fail(h, MOE_W4A16_ERR_UNSUPPORTED, "grouped GEMM path not available");
@@ -464,8 +469,9 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   h->last_path = path;
   const int batches = offload ? (c.max_active + h->xslots - 1) / h->xslots : 0;
   h->last_launches = path == MOE_W4A16_PATH_DECODE_FUSED ? 1
-                     : path == MOE_W4A16_PATH_OFFLOAD ? route_launches + 2 + 3 * batches
-                     : route_launches + (path == MOE_W4A16_PATH_GEMM ? 4 : 2);
+                     : path == MOE_W4A16_PATH_OFFLOAD ? route_launches + !route_gathers + 1 + 3 * batches
+                     : path == MOE_W4A16_PATH_GEMM    ? route_launches + !route_gathers + 3
+                                                      : route_launches + 2;
   return MOE_W4A16_OK;
 }
 

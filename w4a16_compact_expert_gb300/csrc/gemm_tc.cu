@@ -10,8 +10,9 @@
 //   producer warp : 4-D TMA loads fetch the int4 chunks of the 8 row tiles of
 //                   each A matrix (and, at scale-block starts, their block
 //                   scales) into a raw ring; the token rows of B come as 2-D
-//                   TMA tiles, 128-byte swizzled (x gathered into sorted-row
-//                   order by a small kernel for gate/up; h for down)
+//                   TMA tiles, 128-byte swizzled (for gate/up x rows in
+//                   sorted-row order, copied there by the router or by a small
+//                   kernel; h for down)
 //   dequant warps : int4 -> FP16 (nearest q*s) written into a 128-byte
 //                   swizzled K-major A ring (the only place an expanded value
 //                   exists: one 64-wide K step of 2 x 128 rows, per CTA)
@@ -660,7 +661,8 @@ PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slot
   return pm;
 }
 
-cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_t st, const StageEvents& se) {
+cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, bool gathered, cudaStream_t st,
+                                const StageEvents& se) {
   if (!gemm_shapes_supported(c.H, c.I) || !pm.ok) return cudaErrorNotSupported;
   const uint64_t P = (uint64_t)c.T * c.k;
   CUtensorMap mx, mh;
@@ -670,7 +672,8 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_
   if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, false>, Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = c.num_sms > 0 ? c.num_sms : 148;
-  e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
+  if (!gathered)
+    e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 1, st);
   if (e == cudaSuccess)
     e = launch_pdl(grouped_gemm_kernel<true, false>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
@@ -715,7 +718,8 @@ DenseMaps make_dense_maps(const __half* xpool, int H, int I, int xslots) {
 // slots and the dense gate/up and down grouped GEMMs, then the combine.  The
 // number of batches is bounded by max_active on the host; a batch past the
 // active experts exits on the device.
-cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, cudaStream_t st, const StageEvents& se) {
+cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, bool gathered, cudaStream_t st,
+                                   const StageEvents& se) {
   if (!gemm_shapes_supported(c0.H, c0.I) || !dm.ok || c0.xslots < 1) return cudaErrorNotSupported;
   const uint64_t P = (uint64_t)c0.T * c0.k;
   CUtensorMap mx, mh;
@@ -725,7 +729,8 @@ cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, cudaSt
   if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, true>, Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = c0.num_sms > 0 ? c0.num_sms : 148;
-  e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c0);
+  if (!gathered)
+    e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c0);
   if (e == cudaSuccess) e = record_stage(se, 1, st);
   const int nb = (c0.max_active + c0.xslots - 1) / c0.xslots;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {

@@ -44,8 +44,9 @@ struct FwdCtx {
   __half* xp;                  // [T*k][H] activations gathered in sorted-row order (prefill)
   __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
-  int32_t* route_hist;         // [ceil(T/8)][E] per 8-token block expert counts, then bases (large-T router)
+  int32_t* route_hist;         // [ceil(T/8) + 1][E] per 8-token block expert counts, then bases; last row: totals
   unsigned* route_counter;     // [1] arrival counter of the large-T router's scan (self-resetting)
+  unsigned long long* route_bar;  // grid-barrier arrivals of the cooperative router (monotonic, a multiple of its grid)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
   unsigned long long* grid_bar;  // grid-barrier arrivals (monotonic, a multiple of the grid between uses)
   unsigned* expert_ready;      // [2][256] per active expert: finished gate/up items, started down items
@@ -61,11 +62,14 @@ struct FwdCtx {
 
 // Device counter block of a handle, in 32-bit words: [0, 2) the 64-bit grid
 // barrier, [2, 2 + H/32) down arrival counters, then [2][256] per-expert
-// readiness counters.  Zero-initialised; every user leaves it zero (the grid
-// barrier: a multiple of the grid size).
-inline size_t counter_words(int H) { return 2 + (size_t)H / 32 + 2 * 256 + 2; }
+// readiness counters, the large-T router's arrival counter, the cooperative
+// router's 64-bit grid barrier (8-byte aligned) and a last word that nothing
+// writes.  Zero-initialised; every user leaves it zero (the grid barriers: a
+// multiple of their grid size).
 // the word after the readiness counters: the large-T router's arrival counter
 inline size_t route_counter_word(int H) { return 2 + (size_t)H / 32 + 2 * 256; }
+inline size_t route_bar_word(int H) { return (route_counter_word(H) + 2) & ~(size_t)1; }
+inline size_t counter_words(int H) { return route_bar_word(H) + 3; }
 // the last word of the counter block: never written by any kernel (the
 // self-test waits on it)
 inline size_t never_set_word(int H) { return counter_words(H) - 1; }
@@ -109,7 +113,10 @@ struct PoolMaps {
   bool ok;
 };
 PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slots);
-cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, cudaStream_t st, const StageEvents& se);
+// gathered: c.xp already holds the x rows in sorted-row order (else the first
+// launch gathers them).
+cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, bool gathered, cudaStream_t st,
+                                const StageEvents& se);
 
 // The offload-qpacked comparison path: each batch of at most xslots active
 // experts is expanded into FP16 execution slots (offload.cu), then the same
@@ -120,7 +127,13 @@ struct DenseMaps {
 };
 DenseMaps make_dense_maps(const __half* xpool, int H, int I, int xslots);
 cudaError_t launch_expand(const FwdCtx& c, cudaStream_t st);   // active experts [c.ub0, c.ub1)
-cudaError_t launch_offload_experts(const FwdCtx& c, const DenseMaps& dm, cudaStream_t st, const StageEvents& se);
+cudaError_t launch_offload_experts(const FwdCtx& c, const DenseMaps& dm, bool gathered, cudaStream_t st,
+                                   const StageEvents& se);
+
+// route.cu, grouped-GEMM family above the single-launch router: the logits
+// kernel, then one cooperative kernel for softmax / top-k, the permutation and
+// the copy of the routed x rows into sorted-row order (c.xp).  Two launches.
+cudaError_t launch_route_gather(const FwdCtx& c, cudaStream_t st);
 
 // route: the largest T handled by the single-launch cluster router
 #define ROUTE_FUSED_MAX_T 64

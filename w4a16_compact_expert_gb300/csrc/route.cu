@@ -374,6 +374,215 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(FwdCtx c) {
   }
 }
 
+// ------------------------------------------- cooperative router (GEMM family)
+// After route_logits_mma_kernel, one cooperative launch (every CTA
+// co-resident) takes the rest of the routing of the grouped-GEMM family:
+//   phase 1  per 8-token block: softmax / top-k (warp per token) and the
+//            block's pair count per expert (route_hist row b);
+//   phase 2  per expert: exclusive scan of its counts over the blocks, in
+//            place, and its total (route_hist row nb);
+//   phase 3  every CTA turns the totals into the expert offsets; CTA 0 also
+//            publishes them with the active-expert lists; per 8-token block,
+//            the stable scatter of its pairs and the copy of its tokens' x
+//            rows to their sorted rows of xp (each x row read once, written k
+//            times).
+// Two bounded grid barriers separate the phases.  Same results as the
+// separate top-k, scan and scatter launches plus the gather kernel.
+
+DEV_INLINE unsigned long long ld_acquire_u64_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One arrival per CTA (thread 0) on a monotonic 64-bit counter, then a poll
+// until it reaches the next multiple of the grid size; false after about 1 s
+// (STATUS_TIMEOUT set).
+DEV_INLINE bool coop_grid_barrier(unsigned long long* ctr, unsigned nblocks, DevStatus* st) {
+  __threadfence();
+  const unsigned long long old = atomicAdd(ctr, 1ull);
+  const unsigned long long target = (old / nblocks + 1ull) * nblocks;
+  const long long t0 = clock64();
+  while (ld_acquire_u64_gpu(ctr) < target) {
+    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence();
+  return true;
+}
+
+__global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
+  __shared__ float lg[8][256];
+  __shared__ int cnt[8][256];   // phase 1: row 0 = the block's counts; phase 3: per 32-pair chunk
+  __shared__ int s_off[256];
+  __shared__ int s_pos[256];
+  __shared__ int warp_tot[8];
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int T = c.T, E = c.E, k = c.k, nb = (T + 7) / 8, G = (int)gridDim.x;
+  if (tid == 0) s_ok = 1;
+
+  // ---------------------------------------------- phase 1: top-k, counts
+  for (int b = blockIdx.x; b < nb; b += G) {
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) cnt[0][e] = 0;
+    const int t = b * 8 + w;
+    if (t < T) {
+      for (int e = lane; e < E; e += 32) {
+        float sum = 0.f;
+        for (int ks0 = 0; ks0 < c.ksplit; ks0 += 8) {   // 8 loads in flight, summed in slice order
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            v[i] = ks0 + i < c.ksplit ? c.logit_part[((size_t)(ks0 + i) * T + t) * E + e] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sum += v[i];
+        }
+        lg[w][e] = sum;
+      }
+      float r = 1.f;
+      if (c.flags & 2u) {
+        float ss = 0.f;
+        for (int ks = 0; ks < c.ksplit; ++ks) ss += c.ss_part[(size_t)ks * T + t];
+        r = prenorm_scale(ss, c.H);
+        if (lane == 0) c.rnorm[t] = r;
+      }
+      __syncwarp();
+      topk_token(c, t, lg[w], r, nullptr);
+    }
+    __syncthreads();   // the block's ids (global) are visible to the whole CTA
+    const int p0 = b * 8 * k, p1 = min(T, b * 8 + 8) * k;
+    for (int p = p0 + tid; p < p1; p += 256) atomicAdd(&cnt[0][c.ids[p]], 1);   // counts: order-free
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) c.route_hist[(size_t)b * E + e] = cnt[0][e];
+  }
+  __syncthreads();
+  if (tid == 0 && !coop_grid_barrier(c.route_bar, (unsigned)G, c.status)) s_ok = 0;
+  __syncthreads();
+  if (!s_ok) return;
+
+  // ---------------------------------------------- phase 2: per-expert scan
+  const int per = (nb + 255) / 256;   // consecutive blocks per thread
+  for (int e = blockIdx.x; e < E; e += G) {
+    const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+    int loc = 0;
+    for (int bb = b0; bb < b1; ++bb) loc += __ldcg(&c.route_hist[(size_t)bb * E + e]);
+    int incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int ww = 0; ww < w; ++ww) before += warp_tot[ww];
+    int run = before + incl - loc;   // exclusive prefix of this thread's first block
+    for (int bb = b0; bb < b1; ++bb) {
+      const int v = __ldcg(&c.route_hist[(size_t)bb * E + e]);
+      c.route_hist[(size_t)bb * E + e] = run;
+      run += v;
+    }
+    if (tid == 255) c.route_hist[(size_t)nb * E + e] = before + incl;   // the expert's total
+    __syncthreads();   // warp_tot reuse
+  }
+  __syncthreads();
+  if (tid == 0 && !coop_grid_barrier(c.route_bar, (unsigned)G, c.status)) s_ok = 0;
+  __syncthreads();
+  if (!s_ok) return;
+
+  // ---------------------------------------------- phase 3: offsets, scatter, x rows
+  if (w == 0) {   // totals -> exclusive offsets (every CTA); CTA 0 publishes them and the active lists
+    const bool pub = blockIdx.x == 0;
+    int n = 0, tiles = 0, base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int ex = e0 + lane;
+      const int ce = ex < E ? __ldcg(&c.route_hist[(size_t)nb * E + ex]) : 0;
+      int ci = ce;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, ci, o);
+        if (lane >= o) ci += v;
+      }
+      const int off = base + ci - ce;
+      if (ex < E) s_off[ex] = off;
+      if (pub) {
+        const int slot = ce > 0 ? c.table[ex] : -1;
+        const bool act = ce > 0 && slot >= 0;
+        if (ce > 0 && slot < 0) {
+          atomicAdd(&c.status->miss, (unsigned long long)ce);
+          atomicOr(&c.status->flags, STATUS_MISS);
+        }
+        const unsigned am = __ballot_sync(kFull, act);
+        const int pos = n + __popc(am & ((1u << lane) - 1u));
+        const int ntl = act ? (ce + c.tile_tokens - 1) / c.tile_tokens : 0;
+        int ti = ntl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(kFull, ti, o);
+          if (lane >= o) ti += v;
+        }
+        if (ex < E) c.offsets[ex] = off;
+        if (act) {
+          c.act_expert[pos] = ex;
+          c.act_slot[pos] = slot;
+          c.act_start[pos] = off;
+          c.act_count[pos] = ce;
+          c.act_tile[pos] = tiles + ti - ntl;
+        }
+        n += __popc(am);
+        tiles += __shfl_sync(kFull, ti, 31);
+      }
+      base += __shfl_sync(kFull, ci, 31);
+    }
+    if (pub && lane == 0) {
+      c.offsets[E] = base;
+      *c.n_active = n;
+      c.act_tile[n] = tiles;
+    }
+  }
+  const int vpr = c.H / 8;   // 16-byte vectors per x row
+  for (int b = blockIdx.x; b < nb; b += G) {
+    __syncthreads();   // s_off ready; cnt, s_pos reuse
+    const int p0 = b * 8 * k, p1 = min(T, b * 8 + 8) * k;
+    const int nch = (p1 - p0 + 31) / 32;   // <= 8 (k <= 32)
+    for (int i = tid; i < nch * E; i += 256) cnt[i / E][i % E] = 0;
+    __syncthreads();
+    int e = -1 - lane, rank = 0;
+    const int p = p0 + w * 32 + lane;
+    if (w < nch) {
+      e = p < p1 ? c.ids[p] : -1 - lane;
+      const unsigned peers = __match_any_sync(kFull, e);
+      rank = __popc(peers & ((1u << lane) - 1u));
+      if (p < p1 && rank == 0) cnt[w][e] = __popc(peers);
+    }
+    __syncthreads();
+    if (w < nch && p < p1) {
+      int r = rank;
+      for (int ch = 0; ch < w; ++ch) r += cnt[ch][e];
+      const int pos = s_off[e] + __ldcg(&c.route_hist[(size_t)b * E + e]) + r;
+      c.sorted[pos] = p;
+      c.p2r[p] = pos;
+      s_pos[p - p0] = pos;
+    }
+    __syncthreads();
+    const int ntok = min(8, T - b * 8);
+    for (int v = tid; v < vpr; v += 256) {
+      uint4 xv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < ntok) xv[j] = __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)(b * 8 + j) * c.H) + v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < ntok)
+          for (int kk = 0; kk < k; ++kk) reinterpret_cast<uint4*>(c.xp + (size_t)s_pos[j * k + kk] * c.H)[v] = xv[j];
+    }
+  }
+}
+
 }  // namespace
 
 bool route_single_launch(const FwdCtx& c) { return route_cluster_smem(c.T, c.E, c.H, c.k) <= 200 * 1024; }
@@ -398,4 +607,33 @@ cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
   if (e == cudaSuccess) e = launch_pdl(route_scan_kernel, dim3(c.E), dim3(256), 0, st, 1, cc);
   if (e == cudaSuccess) e = launch_pdl(route_scatter_kernel, dim3((c.T + 7) / 8), dim3(256), 0, st, 1, cc);
   return e;
+}
+
+cudaError_t launch_route_gather(const FwdCtx& c, cudaStream_t st) {
+  FwdCtx cc = c;
+  cc.ksplit = (c.H + kRouteKC - 1) / kRouteKC;
+  const size_t lsmem = (size_t)2 * kRouteTile * (kRouteKC + 8) * sizeof(__half);
+  cudaError_t e = opt_in_smem((const void*)route_logits_mma_kernel, lsmem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;   // all CTAs of the cooperative launch must be co-resident
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel, 256, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1 || c.num_sms < 1) return cudaErrorNotSupported;
+  // one grid size for every T (grid-stride loops over the blocks): the
+  // barrier counter stays a multiple of it from launch to launch
+  const int G = c.num_sms * (per_sm >= 2 ? 2 : 1);
+  const dim3 grid((c.T + kRouteTile - 1) / kRouteTile, (c.E + kRouteTile - 1) / kRouteTile, cc.ksplit);
+  e = launch_pdl(route_logits_mma_kernel, grid, dim3(128), lsmem, st, 1, cc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_coop_kernel, cc);
 }
