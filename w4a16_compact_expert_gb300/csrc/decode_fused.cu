@@ -38,6 +38,8 @@
 // (its remaining arithmetic runs on whatever shared memory holds, and the
 // status marks the forward void), and the producer lets its copies land
 // before the CTA exits.
+#include <atomic>
+
 #include "gemv_dev.cuh"
 #include "route_dev.cuh"
 
@@ -471,6 +473,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     for (int q = 0; q < NG; ++q) s_head[q] = s_tail[q] = 0;
     mbar_init(&xbar, 1);
     fence_mbar_init();
+  }
+  // everything above is CTA-local: it overlaps the tail of the preceding
+  // kernel (programmatic dependent launch); x, the table and the counters are
+  // read only after that kernel has completed
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
     // the T token rows of x, staged once (padded rows) for every gate/up item
     // of this CTA; the copies run while the router phase computes
     mbar_expect_tx(&xbar, (uint32_t)T * H * 2);
@@ -914,12 +923,25 @@ cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  // programmatic dependent launch: the launch and the CTA-local prologue
+  // overlap the preceding kernel (all CTAs still co-reside: the preceding
+  // kernel never waits on this one)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+  static std::atomic<int> pdl_ok{1};   // cleared if the driver refuses the pair of attributes
+  cfg.numAttrs = pdl_ok.load() ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+  if (e != cudaSuccess && cfg.numAttrs == 2) {
+    cudaGetLastError();
+    pdl_ok.store(0);
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+  }
+  return e;
 }
 
 }  // namespace

@@ -20,7 +20,7 @@
 //                   matrix into the two 256-column halves of one TMEM
 //                   accumulator and commits stage releases
 //   epilogue      : tcgen05.ld of the accumulator; gate/up: h = SiLU(g) * u
-//                   rounded to FP16; down: y [pair][H] FP32.  Split over the 4
+//                   rounded to FP16; down: y [pair][H] FP16.  Split over the 4
 //                   epilogue warps and the 8 dequant warps, a third each
 // A last kernel gathers out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order.
 // Every wait is bounded (status word + early exit), nothing spins forever.
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nacc = 1;   // one accumulator: the two A matrices' halves fill the 512 columns
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
-  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP32) of
+  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP16) of
   // rows m0 + row (first accumulator half) and m0 + 128 + row (second).  The
   // single accumulator puts the epilogue on the MMA's critical path: it is
   // split over the 4 epilogue warps and the 8 dequant warps (which wait for the
@@ -263,9 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
           } else {
-            float* yr = c.ybuf + (size_t)pair * c.H + et.m0 + row;
-            yr[0] = __uint_as_float(va[j]);
-            yr[kMTile] = __uint_as_float(vb[j]);
+            // the expert's output rounded once to FP16 (an activation), the
+            // combine then sums the k ranks in FP32
+            __half* yr = reinterpret_cast<__half*>(c.ybuf) + (size_t)pair * c.H + et.m0 + row;
+            yr[0] = __float2half_rn(__uint_as_float(va[j]));
+            yr[kMTile] = __float2half_rn(__uint_as_float(vb[j]));
           }
         }
       }
@@ -513,59 +515,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order j, FP32, then FP16.
-// A CTA covers 1024 hidden values of one token (4 per thread); the token's
-// weights (0 for an absent expert) are read once into shared memory so that
-// the y loads of all ranks are independent.
+// A CTA covers 2048 hidden values of one token (8 per thread, 16-byte loads
+// of the FP16 y rows); the token's weights (0 for an absent expert) are read
+// once into shared memory so that the y loads of all ranks are independent.
 __global__ void __launch_bounds__(256) combine_kernel(FwdCtx c) {
   __shared__ float ws[32];
   pdl_wait();
   pdl_trigger();
   const int H = c.H, k = c.k;
-  const int blocks_per_tok = (H / 4 + 255) / 256;
+  const int blocks_per_tok = (H / 8 + 255) / 256;
   const int t = blockIdx.x / blocks_per_tok;
-  const int v = (blockIdx.x % blocks_per_tok) * 256 + threadIdx.x;   // float4 index inside the row
+  const int v = (blockIdx.x % blocks_per_tok) * 256 + threadIdx.x;   // 8-value vector inside the row
   if (threadIdx.x < k) {
     const int p = t * k + threadIdx.x;
     ws[threadIdx.x] = c.table[c.ids[p]] >= 0 ? c.topw[p] : 0.f;
   }
   __syncthreads();
-  if (v >= H / 4) return;
-  float acc[4];
+  if (v >= H / 8) return;
+  float acc[8];
   if (c.flags & 1u) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(c.x + (size_t)t * H + v * 4);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));
-    acc[0] = a.x;
-    acc[1] = a.y;
-    acc[2] = b.x;
-    acc[3] = b.y;
+    const uint4 xv = *reinterpret_cast<const uint4*>(c.x + (size_t)t * H + v * 8);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[i]));
+      acc[2 * i] = f.x;
+      acc[2 * i + 1] = f.y;
+    }
   } else {
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   }
+  const __half* yh = reinterpret_cast<const __half*>(c.ybuf);   // [pair][H] FP16
   for (int j0 = 0; j0 < k; j0 += 8) {
-    float4 y[8];
+    uint4 y[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int j = j0 + u;
-      y[u] = (j < k && ws[j] != 0.f) ? __ldcs(reinterpret_cast<const float4*>(c.ybuf + ((size_t)t * k + j) * H) + v)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      y[u] = (j < k && ws[j] != 0.f) ? __ldcs(reinterpret_cast<const uint4*>(yh + ((size_t)t * k + j) * H) + v)
+                                     : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int j = j0 + u;
       if (j < k && ws[j] != 0.f) {
         const float w = ws[j];
-        acc[0] = fmaf(w, y[u].x, acc[0]);
-        acc[1] = fmaf(w, y[u].y, acc[1]);
-        acc[2] = fmaf(w, y[u].z, acc[2]);
-        acc[3] = fmaf(w, y[u].w, acc[3]);
+        const uint32_t yw[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&yw[i]));
+          acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+        }
       }
     }
   }
-  uint2 o;
-  *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(acc[0], acc[1]);
-  *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(acc[2], acc[3]);
-  *reinterpret_cast<uint2*>(c.out + (size_t)t * H + v * 4) = o;
+  uint4 o;
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h2 = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+    ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  *reinterpret_cast<uint4*>(c.out + (size_t)t * H + v * 8) = o;
 }
 
 // xp[r] = x[sorted[r] / k]: activations in sorted-row order.  A CTA copies 8
@@ -684,7 +696,7 @@ cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, bool gather
                    pm.q[2], pm.sc[2], pm.sc[2]);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c);
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 8 + 255) / 256))), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }
@@ -748,7 +760,7 @@ cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, bool g
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel, dim3((unsigned)(c0.T * ((c0.H / 4 + 255) / 256))), dim3(256), 0, st, 1, c0);
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c0.T * ((c0.H / 8 + 255) / 256))), dim3(256), 0, st, 1, c0);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }

@@ -43,7 +43,7 @@ struct FwdCtx {
   // expert workspaces
   __half* xp;                  // [T*k][H] activations gathered in sorted-row order (prefill)
   __half* hbuf;                // [T*k][I] SiLU*up in sorted-row order
-  float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order
+  float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order (FP32; FP16 on the grouped-GEMM path)
   int32_t* route_hist;         // [ceil(T/8) + 1][E] per 8-token block expert counts, then bases; last row: totals
   unsigned* route_counter;     // [1] arrival counter of the large-T router's scan (self-resetting)
   unsigned long long* route_bar;  // grid-barrier arrivals of the cooperative router (monotonic, a multiple of its grid)
