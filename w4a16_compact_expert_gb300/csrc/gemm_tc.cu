@@ -156,9 +156,10 @@ DEV_INLINE void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
       : "memory");
 }
 
-DEV_INLINE void st_shared_v2_b32(uint32_t addr, uint32_t v0, uint32_t v1) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v0), "r"(v1) : "memory");
+DEV_INLINE void st_shared_v4_b32(uint32_t addr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v0), "r"(v1), "r"(v2), "r"(v3) : "memory");
 }
+
 
 // DENSE: the offload-qpacked comparison.  A comes as FP16 tiles of the
 // execution slots of the active experts [c.ub0, c.ub1) (tmA0 / tmA1: 3-D maps,
@@ -458,13 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sw = (uint32_t)(row & 7);
             const uint32_t w4[4] = {q[m][tt].x, q[m][tt].y, q[m][tt].z, q[m][tt].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t a[4];
-              dequant_word(w4[j], slo[m][tt], shi[m][tt], a);
-              // K values cq*16 + 4j .. + 3 of the chunk: 16-byte unit 2 cq + j/2, bytes (j & 1) * 8 ..
-              const uint32_t cu = (((uint32_t)(2 * cq + (j >> 1)) ^ sw) << 4) + (uint32_t)(j & 1) * 8u;
-              st_shared_v2_b32(rlo + cu, a[0], a[2]);
-              st_shared_v2_b32(rhi + cu, a[1], a[3]);
+            for (int h = 0; h < 2; ++h) {
+              // K values cq*16 + 8h .. + 7 of the chunk fill the 16-byte swizzle
+              // unit 2 cq + h of rows g and g + 8 (words 2h, 2h + 1: 4 K each).
+              // One 16-byte store per row: each 8-lane phase then covers the 8
+              // units of its rows once (no bank conflicts).
+              uint32_t a0[4], a1[4];
+              dequant_word(w4[2 * h], slo[m][tt], shi[m][tt], a0);
+              dequant_word(w4[2 * h + 1], slo[m][tt], shi[m][tt], a1);
+              const uint32_t cu = ((uint32_t)(2 * cq + h) ^ sw) << 4;
+              st_shared_v4_b32(rlo + cu, a0[0], a0[2], a1[0], a1[2]);
+              st_shared_v4_b32(rhi + cu, a0[1], a0[3], a1[1], a1[3]);
             }
           }
         }
