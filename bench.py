@@ -405,7 +405,8 @@ def stage_times(wl, force, stream):
 
 
 def e2e_rate(wl, force, steps, world, local_rank):
-    """Same metric through forward_host: pinned host x in, host out, copies timed."""
+    """Same metric through the host-buffer entry point (forward_host_async):
+    pinned host x in, host out, copies and the per-step synchronisation timed."""
     import torch
     T, H = wl.T, wl.shape.H
     if wl.chain:
@@ -415,12 +416,16 @@ def e2e_rate(wl, force, steps, world, local_rank):
     oh = [torch.empty(T, H, dtype=torch.float16).pin_memory() for _ in range(2 if wl.chain else wl.L)]
 
     def one(i):
+        # every layer's H2D copy, forward and D2H copy enqueued on one stream
+        # (stream order chains a layer's host output into the next layer's
+        # input), then one synchronisation: the step's outputs are on the host
         for l, m in enumerate(wl.layers):
             if wl.chain:
                 src = xh[i % ROTATE] if l == 0 else oh[(l - 1) % 2]
-                m.forward_host(src, wl.rws[l], wl.biases[l], wl.flags | force, out_host=oh[l % 2])
+                m.forward_host_async(src, wl.rws[l], oh[l % 2], wl.biases[l], wl.flags | force)
             else:
-                m.forward_host(xh[l][i % ROTATE], wl.rws[l], wl.biases[l], wl.flags | force, out_host=oh[l])
+                m.forward_host_async(xh[l][i % ROTATE], wl.rws[l], oh[l], wl.biases[l], wl.flags | force)
+        torch.cuda.synchronize()
 
     for i in range(2):
         one(i)

@@ -162,6 +162,20 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_host(moe_w4a16_handle* h, const
                                         const void* router_w, const float* bias, uint32_t flags,
                                         void* out_host, moe_w4a16_stream_t stream);
 
+/* The same as moe_w4a16_forward_host without the final synchronisation: the
+ * H2D copy, the forward and the D2H copy are enqueued on `stream` and the call
+ * returns.  out_host holds the result once the stream has reached that point
+ * (cudaStreamSynchronize or an event); x_host must stay unchanged until then.
+ * Calls on one handle reuse its device staging buffers in stream order, so a
+ * later call on the same stream may follow at once.  Host buffers must be
+ * page-locked for the copies to run asynchronously (pageable buffers are
+ * still correct, the driver then stages them synchronously).  Errors as for
+ * moe_w4a16_forward; a failed copy enqueue returns ERR_CUDA. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_host_async(moe_w4a16_handle* h, const void* x_host, int32_t T,
+                                                            const void* router_w, const float* bias,
+                                                            uint32_t flags, void* out_host,
+                                                            moe_w4a16_stream_t stream);
+
 /* Synchronises the handle's device, reads and clears the device status word.
  * *miss_count (may be NULL) receives the number of routed token-expert pairs
  * whose expert had no slot since the last call.  Returns ERR_TIMEOUT if a

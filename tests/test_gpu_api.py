@@ -126,6 +126,29 @@ def test_forward_host_matches_forward(tiny):
     assert np.array_equal(out, oh.astype(np.float64))
 
 
+def test_forward_host_async_chain_matches_forward(tiny):
+    """Three enqueued host-buffer forwards on one handle and one stream, each
+    reading the previous one's host output (stream order), then one
+    synchronisation: equal to the device forwards chained the same way."""
+    import torch
+    x = synth.draw_x(4, 12, 256)
+    m = gp.make_handle(tiny, 16)
+    try:
+        rw = gp.to_dev(tiny.router_w)
+        hosts = [torch.from_numpy(x).pin_memory()] + [torch.empty(12, 256, dtype=torch.float16).pin_memory()
+                                                      for _ in range(3)]
+        for i in range(3):
+            m.forward_host_async(hosts[i], rw, hosts[i + 1], None, F.RESIDUAL)
+        torch.cuda.synchronize()
+        ref = x
+        for i in range(3):
+            out, _ = gp.gpu_forward(m, tiny, ref.astype(np.float16), F.RESIDUAL)
+            ref = out
+    finally:
+        m.close()
+    assert np.array_equal(hosts[3].numpy().astype(np.float64), ref)
+
+
 def test_argument_errors(tiny):
     import torch
     m = gp.make_handle(tiny, 8)

@@ -483,6 +483,18 @@ int32_t moe_w4a16_last_path(const moe_w4a16_handle* h, int32_t* launches) {
 
 moe_w4a16_status moe_w4a16_forward_host(moe_w4a16_handle* h, const void* x_host, int32_t T, const void* router_w,
                                         const float* bias, uint32_t flags, void* out_host, moe_w4a16_stream_t stream) {
+  const moe_w4a16_status s = moe_w4a16_forward_host_async(h, x_host, T, router_w, bias, flags, out_host, stream);
+  if (s != MOE_W4A16_OK || T == 0) return s;
+  DeviceGuard dg(h->cfg.device);
+  if (!dg.ok) return fail(h, MOE_W4A16_ERR_CUDA, "cudaSetDevice failed");
+  const cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "forward_host synchronize");
+  return MOE_W4A16_OK;
+}
+
+moe_w4a16_status moe_w4a16_forward_host_async(moe_w4a16_handle* h, const void* x_host, int32_t T,
+                                              const void* router_w, const float* bias, uint32_t flags, void* out_host,
+                                              moe_w4a16_stream_t stream) {
   if (!h) return MOE_W4A16_ERR_INVALID_ARG;
   if (T < 0 || T > h->cfg.max_tokens) return fail(h, MOE_W4A16_ERR_INVALID_ARG, "T outside [0, max_tokens]");
   if (T == 0) return MOE_W4A16_OK;
@@ -497,7 +509,6 @@ moe_w4a16_status moe_w4a16_forward_host(moe_w4a16_handle* h, const void* x_host,
                                          nullptr, nullptr, stream);
   if (s != MOE_W4A16_OK) return s;
   e = cudaMemcpyAsync(out_host, h->out_dev, bytes, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(h, e, "forward_host D2H");
   return MOE_W4A16_OK;
 }

@@ -21,7 +21,7 @@ STATUS_NAMES = ["OK", "ERR_INVALID_ARG", "ERR_CUDA", "ERR_OOM", "ERR_NOT_PACKED"
 RESIDUAL, PRENORM, FORCE_GEMV, FORCE_GEMM, UNFUSED, OFFLOAD = 1, 2, 4, 8, 16, 32
 
 EXPORTED = ["moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack_experts", "moe_w4a16_set_slot_table",
-            "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_get_status", "moe_w4a16_last_error",
+            "moe_w4a16_forward", "moe_w4a16_forward_host", "moe_w4a16_forward_host_async", "moe_w4a16_get_status", "moe_w4a16_last_error",
             "moe_w4a16_slot_bytes", "moe_w4a16_get_gemv_max_tokens", "moe_w4a16_set_gemv_max_tokens",
             "moe_w4a16_set_stage_events", "moe_w4a16_last_path", "moe_w4a16_route_noalloc",
             "moe_w4a16_cache_create", "moe_w4a16_cache_destroy", "moe_w4a16_cache_acquire",
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_w4a16_set_slot_table.argtypes = [vp, vp, vp]
     lib.moe_w4a16_forward.argtypes = [vp, vp, i32, vp, vp, u32, vp, vp, vp, vp, vp, vp]
     lib.moe_w4a16_forward_host.argtypes = [vp, vp, i32, vp, vp, u32, vp, vp]
+    lib.moe_w4a16_forward_host_async.argtypes = [vp, vp, i32, vp, vp, u32, vp, vp]
     lib.moe_w4a16_get_status.argtypes = [vp, i64p]
     lib.moe_w4a16_last_error.argtypes = [vp]
     lib.moe_w4a16_last_error.restype = ctypes.c_char_p
@@ -230,6 +231,15 @@ class MoELayer:
             out_host = np.empty_like(x_host)
         self._check(self.lib.moe_w4a16_forward_host(self.h, _ptr(x_host), T, _ptr(router_w), _ptr(bias), flags,
                                                     _ptr(out_host), _stream(stream)))
+        return out_host
+
+    def forward_host_async(self, x_host, router_w, out_host, bias=None, flags: int = 0, stream=None):
+        """Enqueues H2D of x_host, the forward and D2H into out_host on `stream`
+        and returns; out_host is valid after the stream synchronises.  Both
+        host buffers should be pinned."""
+        T = int(x_host.shape[0])
+        self._check(self.lib.moe_w4a16_forward_host_async(self.h, _ptr(x_host), T, _ptr(router_w), _ptr(bias),
+                                                          flags, _ptr(out_host), _stream(stream)))
         return out_host
 
     def set_stage_events(self, events):
