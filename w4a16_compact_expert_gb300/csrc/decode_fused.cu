@@ -116,6 +116,25 @@ DEV_INLINE unsigned ld_acquire_u32(const unsigned* p) {
 // Bounded barrier over all CTAs of the grid, called by one thread per CTA:
 // one arrival on a monotonic 64-bit counter, then a poll until it reaches the
 // next multiple of the grid size (every launch leaves it at a multiple).
+// Split into an arrival and a wait, so that a CTA can do local work between.
+DEV_INLINE unsigned long long grid_arrive(unsigned long long* ctr, unsigned nblocks) {
+  __threadfence();
+  const unsigned long long old = atomicAdd(ctr, 1ull);
+  return (old / nblocks + 1ull) * nblocks;
+}
+
+DEV_INLINE bool grid_wait(const unsigned long long* ctr, unsigned long long target, DevStatus* st) {
+  const long long t0 = clock64();
+  while (ld_acquire_u64(ctr) < target) {
+    if (clock64() - t0 > MOE_WAIT_CYCLES) {
+      atomicOr(&st->flags, STATUS_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 DEV_INLINE bool grid_barrier(unsigned long long* ctr, unsigned nblocks, DevStatus* st) {
   __threadfence();
   const unsigned long long old = atomicAdd(ctr, 1ull);
@@ -510,7 +529,20 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     }
   }
   __syncthreads();
-  if (tid == 0 && !grid_barrier(c.grid_bar, (unsigned)G, c.status)) s_ok = 0;
+  // arrive at the routing barrier, then (while the other CTAs arrive) the
+  // per-chunk prefix sums of the staged x rows, then wait
+  unsigned long long bar_target = 0;
+  if (tid == 0) {
+    bar_target = grid_arrive(c.grid_bar, (unsigned)G);
+    if (!mbar_wait_bounded(&xbar, 0, c.status)) s_ok = 0;   // x rows landed
+  }
+  __syncthreads();
+  if (s_ok) {
+    chunk_sums(sb_x, xcache, H + 8, T, H / 64, tid, kNW * 32);
+    __syncthreads();
+    chunk_prefix(sb_x, T, H / 64, tid, kNW * 32);
+  }
+  if (tid == 0 && s_ok && !grid_wait(c.grid_bar, bar_target, c.status)) s_ok = 0;
   __syncthreads();
   if (!s_ok) {
     if (tid == 0) mbar_wait_bounded(&xbar, 0, c.status);   // let the x copies land
@@ -731,7 +763,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     }
   }
   named_sync(1, kCW * 32);
-  if (tid == 0 && !mbar_wait_bounded(&xbar, 0, c.status)) s_abort = 1;
   if (b == 0) {   // publish the routing (debug outputs, rnorm)
     for (int i = tid; i < P; i += kCW * 32) {
       c.ids[i] = r_ids[i];
@@ -742,10 +773,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     if (c.flags & 2u)
       for (int i = tid; i < T; i += kCW * 32) c.rnorm[i] = r_rnorm[i];
   }
-  named_sync(1, kCW * 32);
-  chunk_sums(sb_x, xcache, H + 8, T, H / 64, tid, kCW * 32);   // x rows landed (xbar) before the barrier
-  named_sync(1, kCW * 32);
-  chunk_prefix(sb_x, T, H / 64, tid, kCW * 32);
   named_sync(1, kCW * 32);
   if (U == 0) {   // every routed expert is absent: out = residual or 0
     for (int i = b * kCW * 32 + tid; i < T * H; i += G * kCW * 32)
