@@ -212,12 +212,13 @@ def test_device_source_pack_matches_host_pack(tiny):
     (4, F.UNFUSED, F.PATH_DECODE, 3),
     (4, F.FORCE_GEMM, F.PATH_GEMM, 5),
     (100, F.FORCE_GEMM, F.PATH_GEMM, 5),
-    (100, F.FORCE_GEMV, F.PATH_DECODE, 6),
+    (100, F.FORCE_GEMV, F.PATH_DECODE, 4),
+    (12, F.UNFUSED, F.PATH_DECODE, 4),
 ])
 def test_last_path_reports_kernels(tiny, T, flags, path, launches):
     """The reported path and launch count follow the dispatch rules: one
-    cooperative kernel for small T, a one-kernel router up to 64 tokens, a
-    four-kernel router above (two kernels that also gather the x rows on the
+    cooperative kernel for small T, a one-kernel router up to 8 tokens, a
+    two-kernel router above (which also gathers the x rows on the
     grouped-GEMM path)."""
     m = gp.make_handle(tiny, 128)
     try:

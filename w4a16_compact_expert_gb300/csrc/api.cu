@@ -435,13 +435,13 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
   const bool single_route = fused_route && route_single_launch(c);
-  // the grouped-GEMM family above the single-launch router: logits + one
-  // cooperative kernel that also copies the x rows into sorted-row order
+  // above the single-launch router: logits + one cooperative kernel, which on
+  // the grouped-GEMM family also copies the x rows into sorted-row order
   const bool route_gathers = gemm && !single_route;
-  const int route_launches = single_route ? 1 : route_gathers ? 2 : 4;
+  const int route_launches = single_route ? 1 : 2;
   int32_t path = offload ? MOE_W4A16_PATH_OFFLOAD : gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
-  if (e == cudaSuccess && !fused) e = route_gathers ? launch_route_gather(c, st) : launch_route(c, fused_route, st);
+  if (e == cudaSuccess && !fused) e = single_route ? launch_route(c, true, st) : launch_route_gather(c, gemm, st);
   if (e == cudaSuccess && !gemm) e = record_stage(h->events, 1, st);   // the GEMM family records it after the gather
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   if (fused) {

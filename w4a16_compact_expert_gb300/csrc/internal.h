@@ -130,13 +130,15 @@ cudaError_t launch_expand(const FwdCtx& c, cudaStream_t st);   // active experts
 cudaError_t launch_offload_experts(const FwdCtx& c, const DenseMaps& dm, bool gathered, cudaStream_t st,
                                    const StageEvents& se);
 
-// route.cu, grouped-GEMM family above the single-launch router: the logits
-// kernel, then one cooperative kernel for softmax / top-k, the permutation and
-// the copy of the routed x rows into sorted-row order (c.xp).  Two launches.
-cudaError_t launch_route_gather(const FwdCtx& c, cudaStream_t st);
+// route.cu, above the single-launch router: the logits kernel, then one
+// cooperative kernel for softmax / top-k and the permutation, and with
+// `gather` the copy of the routed x rows into sorted-row order (c.xp).  Two
+// launches.
+cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st);
 
-// route: the largest T handled by the single-launch cluster router
-#define ROUTE_FUSED_MAX_T 64
+// route: the largest T handled by the single-launch cluster router (its
+// 8 CTAs take about 4 us per 8 tokens; the two-launch router is faster above)
+#define ROUTE_FUSED_MAX_T 8
 
 // gemv.cu: dynamic shared memory of the decode kernels for `rows` staged tokens.
 size_t gemv_smem_gateup(int H, int I, int rows);

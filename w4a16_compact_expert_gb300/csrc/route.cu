@@ -13,7 +13,11 @@
 //              into CTA 0's shared memory (distributed shared memory); after
 //              the cluster barrier CTA 0 finishes softmax/top-k and the
 //              permutation entirely in shared memory.
-//   larger T : logits, top-k (warp per token) and permutation as three launches.
+//   larger T : the tensor-core logits kernel, then either one cooperative
+//              kernel (top-k, scan, scatter and, for the grouped GEMM, the x
+//              rows in sorted order: the forward's router) or three more
+//              launches (top-k, scan, scatter: the allocation-free router,
+//              which has no barrier counter of its own).
 #include "route_dev.cuh"
 
 namespace {
@@ -383,9 +387,9 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(FwdCtx c) {
 //            place, and its total (route_hist row nb);
 //   phase 3  every CTA turns the totals into the expert offsets; CTA 0 also
 //            publishes them with the active-expert lists; per 8-token block,
-//            the stable scatter of its pairs and the copy of its tokens' x
-//            rows to their sorted rows of xp (each x row read once, written k
-//            times).
+//            the stable scatter of its pairs and (when xp is set: the
+//            grouped-GEMM family) the copy of its tokens' x rows to their
+//            sorted rows of xp (each x row read once, written k times).
 // Two bounded grid barriers separate the phases.  Same results as the
 // separate top-k, scan and scatter launches plus the gather kernel.
 
@@ -570,7 +574,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     }
     __syncthreads();
     const int ntok = min(8, T - b * 8);
-    for (int v = tid; v < vpr; v += 256) {
+    for (int v = tid; c.xp && v < vpr; v += 256) {
       uint4 xv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -609,8 +613,9 @@ cudaError_t launch_route(const FwdCtx& c, bool small, cudaStream_t st) {
   return e;
 }
 
-cudaError_t launch_route_gather(const FwdCtx& c, cudaStream_t st) {
+cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st) {
   FwdCtx cc = c;
+  if (!gather) cc.xp = nullptr;
   cc.ksplit = (c.H + kRouteKC - 1) / kRouteKC;
   const size_t lsmem = (size_t)2 * kRouteTile * (kRouteKC + 8) * sizeof(__half);
   cudaError_t e = opt_in_smem((const void*)route_logits_mma_kernel, lsmem);
