@@ -249,10 +249,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_set_gemv_max_tokens(moe_w4a16_handle* h
  * how many kernels it launched (debug-output copies not counted):
  *   MOE_W4A16_PATH_DECODE_FUSED  1 cooperative kernel (routing, permutation,
  *                                gate/up, down and combine in one launch)
- *   MOE_W4A16_PATH_DECODE        router (T <= 8: 1 kernel, above: 2) +
- *                                gate/up + down
- *   MOE_W4A16_PATH_GEMM          router + gather (T <= 8: 1 + 1; above: 2
- *                                kernels that also gather the x rows) +
+ *   MOE_W4A16_PATH_DECODE        router (1 kernel) + gate/up + down
+ *   MOE_W4A16_PATH_GEMM          router + gather (T <= 8: 1 + 1; above: 1
+ *                                kernel that also gathers the x rows) +
  *                                gate/up GEMM + down GEMM + combine
  *   MOE_W4A16_PATH_OFFLOAD       router + gather (as above) + per batch of
  *                                execution slots (expand + dense gate/up GEMM

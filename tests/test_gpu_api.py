@@ -211,15 +211,15 @@ def test_device_source_pack_matches_host_pack(tiny):
     (4, 0, F.PATH_DECODE_FUSED, 1),
     (4, F.UNFUSED, F.PATH_DECODE, 3),
     (4, F.FORCE_GEMM, F.PATH_GEMM, 5),
-    (100, F.FORCE_GEMM, F.PATH_GEMM, 5),
-    (100, F.FORCE_GEMV, F.PATH_DECODE, 4),
-    (12, F.UNFUSED, F.PATH_DECODE, 4),
+    (100, F.FORCE_GEMM, F.PATH_GEMM, 4),
+    (100, F.FORCE_GEMV, F.PATH_DECODE, 3),
+    (12, F.UNFUSED, F.PATH_DECODE, 3),
 ])
 def test_last_path_reports_kernels(tiny, T, flags, path, launches):
     """The reported path and launch count follow the dispatch rules: one
-    cooperative kernel for small T, a one-kernel router up to 8 tokens, a
-    two-kernel router above (which also gathers the x rows on the
-    grouped-GEMM path)."""
+    cooperative kernel for small T, a one-kernel cluster router up to 8
+    tokens, a one-kernel cooperative router above (which also gathers the x
+    rows on the grouped-GEMM path)."""
     m = gp.make_handle(tiny, 128)
     try:
         assert m.last_path() == (F.PATH_NONE, 0)

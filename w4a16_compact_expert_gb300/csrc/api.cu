@@ -435,10 +435,10 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
   c.max_active = ma;
   const bool fused = !gemm && !(flags & MOE_W4A16_UNFUSED) && fused_decode_supported(c, h->max_smem);
   const bool single_route = fused_route && route_single_launch(c);
-  // above the single-launch router: logits + one cooperative kernel, which on
+  // above the single-launch cluster router: one cooperative kernel, which on
   // the grouped-GEMM family also copies the x rows into sorted-row order
   const bool route_gathers = gemm && !single_route;
-  const int route_launches = single_route ? 1 : 2;
+  const int route_launches = 1;
   int32_t path = offload ? MOE_W4A16_PATH_OFFLOAD : gemm ? MOE_W4A16_PATH_GEMM : MOE_W4A16_PATH_DECODE;
   cudaError_t e = record_stage(h->events, 0, st);
   if (e == cudaSuccess && !fused) e = single_route ? launch_route(c, true, st) : launch_route_gather(c, gemm, st);

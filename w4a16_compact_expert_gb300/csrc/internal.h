@@ -46,7 +46,7 @@ struct FwdCtx {
   float* ybuf;                 // [T*k][H] per-pair expert output in flat pair order (FP32; FP16 on the grouped-GEMM path)
   int32_t* route_hist;         // [ceil(T/8) + 1][E] per 8-token block expert counts, then bases; last row: totals
   unsigned* route_counter;     // [1] arrival counter of the large-T router's scan (self-resetting)
-  unsigned long long* route_bar;  // grid-barrier arrivals of the cooperative router (monotonic, a multiple of its grid)
+  unsigned long long* route_bar;  // [2] grid-barrier counters of the cooperative router (monotonic; one grid size each)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
   unsigned long long* grid_bar;  // grid-barrier arrivals (monotonic, a multiple of the grid between uses)
   unsigned* expert_ready;      // [2][256] per active expert: finished gate/up items, started down items
@@ -63,13 +63,13 @@ struct FwdCtx {
 // Device counter block of a handle, in 32-bit words: [0, 2) the 64-bit grid
 // barrier, [2, 2 + H/32) down arrival counters, then [2][256] per-expert
 // readiness counters, the large-T router's arrival counter, the cooperative
-// router's 64-bit grid barrier (8-byte aligned) and a last word that nothing
-// writes.  Zero-initialised; every user leaves it zero (the grid barriers: a
-// multiple of their grid size).
+// router's two 64-bit grid-barrier counters (8-byte aligned) and a last word
+// that nothing writes.  Zero-initialised; every user leaves it zero (the
+// grid barriers: a multiple of their grid size).
 // the word after the readiness counters: the large-T router's arrival counter
 inline size_t route_counter_word(int H) { return 2 + (size_t)H / 32 + 2 * 256; }
 inline size_t route_bar_word(int H) { return (route_counter_word(H) + 2) & ~(size_t)1; }
-inline size_t counter_words(int H) { return route_bar_word(H) + 3; }
+inline size_t counter_words(int H) { return route_bar_word(H) + 5; }
 // the last word of the counter block: never written by any kernel (the
 // self-test waits on it)
 inline size_t never_set_word(int H) { return counter_words(H) - 1; }
@@ -130,14 +130,13 @@ cudaError_t launch_expand(const FwdCtx& c, cudaStream_t st);   // active experts
 cudaError_t launch_offload_experts(const FwdCtx& c, const DenseMaps& dm, bool gathered, cudaStream_t st,
                                    const StageEvents& se);
 
-// route.cu, above the single-launch router: the logits kernel, then one
-// cooperative kernel for softmax / top-k and the permutation, and with
-// `gather` the copy of the routed x rows into sorted-row order (c.xp).  Two
-// launches.
+// route.cu, above the single-launch cluster router: one cooperative kernel
+// for the logits, softmax / top-k and the permutation, and with `gather` the
+// copy of the routed x rows into sorted-row order (c.xp).
 cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st);
 
 // route: the largest T handled by the single-launch cluster router (its
-// 8 CTAs take about 4 us per 8 tokens; the two-launch router is faster above)
+// 8 CTAs take about 4 us per 8 tokens; the cooperative router is faster above)
 #define ROUTE_FUSED_MAX_T 8
 
 // gemv.cu: dynamic shared memory of the decode kernels for `rows` staged tokens.

@@ -13,11 +13,11 @@
 //              into CTA 0's shared memory (distributed shared memory); after
 //              the cluster barrier CTA 0 finishes softmax/top-k and the
 //              permutation entirely in shared memory.
-//   larger T : the tensor-core logits kernel, then either one cooperative
-//              kernel (top-k, scan, scatter and, for the grouped GEMM, the x
-//              rows in sorted order: the forward's router) or three more
-//              launches (top-k, scan, scatter: the allocation-free router,
-//              which has no barrier counter of its own).
+//   larger T : one cooperative kernel (logits on the tensor cores, top-k,
+//              scan, scatter and, for the grouped GEMM, the x rows in sorted
+//              order: the forward's router), or four launches (logits, top-k,
+//              scan, scatter: the allocation-free router, which has no
+//              barrier counter of its own).
 #include "route_dev.cuh"
 
 namespace {
@@ -140,79 +140,88 @@ constexpr int kRouteTile = 64;    // tokens x experts of one logits CTA
 
 // Partial logits of a 64-token x 64-expert tile over one 256-wide K slice on
 // the tensor cores (16x8x16 MMA, FP16 in, FP32 accumulate); the slices are
-// summed in fixed order by the top-k kernel.
-__global__ void __launch_bounds__(128) route_logits_mma_kernel(FwdCtx c) {
-  extern __shared__ __align__(16) uint8_t lsm[];
-  pdl_wait();
-  pdl_trigger();
+// summed in fixed order by the top-k step.  Threads [0, nthr) load (nthr a
+// multiple of 128); warps 0-3 multiply.  sm: 2 x 64 x (256 + 8) halves.
+constexpr int kLogitSmem = 2 * kRouteTile * (kRouteKC + 8) * 2;
+DEV_INLINE void logits_tile(const FwdCtx& c, int tt, int et, int ks, uint8_t* sm, int nthr) {
   constexpr int S = kRouteKC + 8;   // padded row stride (halves): conflict-free fragment reads
-  __half* xs = reinterpret_cast<__half*>(lsm);
+  __half* xs = reinterpret_cast<__half*>(sm);
   __half* ws = xs + kRouteTile * S;
   const int T = c.T, E = c.E, H = c.H;
-  const int t0 = blockIdx.x * kRouteTile, e0 = blockIdx.y * kRouteTile, ks = blockIdx.z;
+  const int t0 = tt * kRouteTile, e0 = et * kRouteTile;
   const int k0 = ks * kRouteKC, kc = min(kRouteKC, H - k0);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, cq = lane & 3;
   const int vpr = kc / 8;   // 16-byte vectors per row
   const int nvec = kRouteTile * vpr;
-  for (int i0 = 0; i0 < nvec; i0 += 8 * 128) {   // 16 independent loads in flight per thread
-    uint4 xv[8], wv[8];
+  if (tid < nthr)
+    for (int i0 = 0; i0 < nvec; i0 += 8 * nthr) {   // 16 independent loads in flight per thread
+      uint4 xv[8], wv[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * 128 + tid;
-      const int r = i / vpr, v = i % vpr;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      xv[u] = (i < nvec && t0 + r < T) ? __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)(t0 + r) * H + k0) + v) : z;
-      wv[u] = (i < nvec && e0 + r < E) ? __ldg(reinterpret_cast<const uint4*>(c.router_w + (size_t)(e0 + r) * H + k0) + v)
-                                       : z;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * 128 + tid;
-      if (i < nvec) {
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * nthr + tid;
         const int r = i / vpr, v = i % vpr;
-        *reinterpret_cast<uint4*>(xs + r * S + v * 8) = xv[u];
-        *reinterpret_cast<uint4*>(ws + r * S + v * 8) = wv[u];
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        xv[u] = (i < nvec && t0 + r < T) ? __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)(t0 + r) * H + k0) + v) : z;
+        wv[u] = (i < nvec && e0 + r < E) ? __ldg(reinterpret_cast<const uint4*>(c.router_w + (size_t)(e0 + r) * H + k0) + v)
+                                         : z;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * nthr + tid;
+        if (i < nvec) {
+          const int r = i / vpr, v = i % vpr;
+          *reinterpret_cast<uint4*>(xs + r * S + v * 8) = xv[u];
+          *reinterpret_cast<uint4*>(ws + r * S + v * 8) = wv[u];
+        }
       }
     }
-  }
   __syncthreads();
-  float acc[8][4];
+  if (w < 4) {
+    float acc[8][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-  const __half* xa = xs + (w * 16 + g) * S + 2 * cq;
-  for (int kk = 0; kk < kc; kk += 16) {
-    uint32_t a[4];
-    a[0] = *reinterpret_cast<const uint32_t*>(xa + kk);
-    a[1] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk);
-    a[2] = *reinterpret_cast<const uint32_t*>(xa + kk + 8);
-    a[3] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk + 8);
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    const __half* xa = xs + (w * 16 + g) * S + 2 * cq;
+    for (int kk = 0; kk < kc; kk += 16) {
+      uint32_t a[4];
+      a[0] = *reinterpret_cast<const uint32_t*>(xa + kk);
+      a[1] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk);
+      a[2] = *reinterpret_cast<const uint32_t*>(xa + kk + 8);
+      a[3] = *reinterpret_cast<const uint32_t*>(xa + 8 * S + kk + 8);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const __half* wb = ws + (nt * 8 + g) * S + kk + 2 * cq;
+        mma_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(wb), *reinterpret_cast<const uint32_t*>(wb + 8));
+      }
+    }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const __half* wb = ws + (nt * 8 + g) * S + kk + 2 * cq;
-      mma_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(wb), *reinterpret_cast<const uint32_t*>(wb + 8));
-    }
-  }
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = t0 + w * 16 + g + (i >= 2 ? 8 : 0), e = e0 + nt * 8 + 2 * cq + (i & 1);
-      if (t < T && e < E) c.logit_part[((size_t)ks * T + t) * E + e] = acc[nt][i];
-    }
-  }
-  if ((c.flags & 2u) && blockIdx.y == 0) {   // PRENORM: partial sums of squares
-    for (int r = w; r < kRouteTile; r += 4) {
-      float s2 = 0.f;
-      for (int kk = lane * 2; kk < kc; kk += 64) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(xs + r * S + kk));
-        s2 = fmaf(f.x, f.x, fmaf(f.y, f.y, s2));
+      for (int i = 0; i < 4; ++i) {
+        const int t = t0 + w * 16 + g + (i >= 2 ? 8 : 0), e = e0 + nt * 8 + 2 * cq + (i & 1);
+        if (t < T && e < E) c.logit_part[((size_t)ks * T + t) * E + e] = acc[nt][i];
       }
-      s2 = warp_sum(s2);
-      if (lane == 0 && t0 + r < T) c.ss_part[(size_t)ks * T + t0 + r] = s2;
+    }
+    if ((c.flags & 2u) && et == 0) {   // PRENORM: partial sums of squares
+      for (int r = w; r < kRouteTile; r += 4) {
+        float s2 = 0.f;
+        for (int kk = lane * 2; kk < kc; kk += 64) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(xs + r * S + kk));
+          s2 = fmaf(f.x, f.x, fmaf(f.y, f.y, s2));
+        }
+        s2 = warp_sum(s2);
+        if (lane == 0 && t0 + r < T) c.ss_part[(size_t)ks * T + t0 + r] = s2;
+      }
     }
   }
+}
+
+__global__ void __launch_bounds__(128) route_logits_mma_kernel(FwdCtx c) {
+  extern __shared__ __align__(16) uint8_t lsm[];
+  pdl_wait();
+  pdl_trigger();
+  logits_tile(c, blockIdx.x, blockIdx.y, blockIdx.z, lsm, 128);
 }
 
 // One warp per token: sums the K slices of its logits (fixed order), then
@@ -378,20 +387,23 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(FwdCtx c) {
   }
 }
 
-// ------------------------------------------- cooperative router (GEMM family)
-// After route_logits_mma_kernel, one cooperative launch (every CTA
-// co-resident) takes the rest of the routing of the grouped-GEMM family:
-//   phase 1  per 8-token block: softmax / top-k (warp per token) and the
-//            block's pair count per expert (route_hist row b);
+// ------------------------------------------- cooperative router
+// One cooperative launch (every CTA co-resident) routes T > 8 tokens:
+//   phase 0  the logits tiles of route_logits_mma_kernel (64 tokens x 64
+//            experts x 256 K each), spread over the grid;
+//   phase 1  per 8-token block: softmax / top-k (warp per token, the K slices
+//            summed in order) and the block's pair count per expert
+//            (route_hist row b);
 //   phase 2  per expert: exclusive scan of its counts over the blocks, in
-//            place, and its total (route_hist row nb);
+//            place, and its total (route_hist row nb); skipped for at most
+//            kDirectBlocks blocks, where phase 3 sums the counts itself;
 //   phase 3  every CTA turns the totals into the expert offsets; CTA 0 also
 //            publishes them with the active-expert lists; per 8-token block,
 //            the stable scatter of its pairs and (when xp is set: the
 //            grouped-GEMM family) the copy of its tokens' x rows to their
 //            sorted rows of xp (each x row read once, written k times).
-// Two bounded grid barriers separate the phases.  Same results as the
-// separate top-k, scan and scatter launches plus the gather kernel.
+// Bounded grid barriers separate the phases.  Same results as the separate
+// logits, top-k, scan and scatter launches plus the gather kernel.
 
 DEV_INLINE unsigned long long ld_acquire_u64_gpu(const unsigned long long* p) {
   unsigned long long v;
@@ -399,8 +411,10 @@ DEV_INLINE unsigned long long ld_acquire_u64_gpu(const unsigned long long* p) {
   return v;
 }
 
-// One arrival per CTA (thread 0) on a monotonic 64-bit counter, then a poll
-// until it reaches the next multiple of the grid size; false after about 1 s
+// Bounded barrier over the grid, called by thread 0 of each CTA: one arrival
+// on a monotonic 64-bit counter, then a poll until it reaches the next
+// multiple of the grid size.  Each counter is only ever used with one grid
+// size, so every launch leaves it at a multiple.  False after about 1 s
 // (STATUS_TIMEOUT set).
 DEV_INLINE bool coop_grid_barrier(unsigned long long* ctr, unsigned nblocks, DevStatus* st) {
   __threadfence();
@@ -418,16 +432,42 @@ DEV_INLINE bool coop_grid_barrier(unsigned long long* ctr, unsigned nblocks, Dev
   return true;
 }
 
+// Up to this many 8-token blocks, every CTA sums the expert counts of the
+// blocks itself (no per-expert scan phase, one grid barrier less), and the
+// grid is one CTA per SM (barrier counter 0); above, two CTAs per SM where
+// they fit (counter 1).
+constexpr int kDirectBlocks = 64;
+
 __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
+  extern __shared__ __align__(16) uint8_t csm[];   // one logits tile (phase 0)
   __shared__ float lg[8][256];
   __shared__ int cnt[8][256];   // phase 1: row 0 = the block's counts; phase 3: per 32-pair chunk
   __shared__ int s_off[256];
+  __shared__ int s_tot[256];    // per expert: pairs routed to it
+  __shared__ int s_base[256];   // per expert: its pairs in blocks before the current one
   __shared__ int s_pos[256];
   __shared__ int warp_tot[8];
   __shared__ int s_ok;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int T = c.T, E = c.E, k = c.k, nb = (T + 7) / 8, G = (int)gridDim.x;
+  const bool direct = nb <= kDirectBlocks;
+  unsigned long long* bar = c.route_bar + (direct ? 0 : 1);   // one grid size per counter
   if (tid == 0) s_ok = 1;
+
+  // ---------------------------------------------- phase 0: logits tiles
+  {
+    const int ntt = (T + kRouteTile - 1) / kRouteTile, net = (E + kRouteTile - 1) / kRouteTile;
+    const int ntiles = ntt * net * c.ksplit;
+    for (int ti = blockIdx.x; ti < ntiles; ti += G) {
+      __syncthreads();   // the previous tile's shared memory is free
+      const int ks = ti % c.ksplit, rest = ti / c.ksplit;
+      logits_tile(c, rest / net, rest % net, ks, csm, 256);
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
+  __syncthreads();
+  if (!s_ok) return;
 
   // ---------------------------------------------- phase 1: top-k, counts
   for (int b = blockIdx.x; b < nb; b += G) {
@@ -441,7 +481,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
           float v[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            v[i] = ks0 + i < c.ksplit ? c.logit_part[((size_t)(ks0 + i) * T + t) * E + e] : 0.f;
+            v[i] = ks0 + i < c.ksplit ? __ldcg(&c.logit_part[((size_t)(ks0 + i) * T + t) * E + e]) : 0.f;
 #pragma unroll
           for (int i = 0; i < 8; ++i) sum += v[i];
         }
@@ -450,7 +490,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
       float r = 1.f;
       if (c.flags & 2u) {
         float ss = 0.f;
-        for (int ks = 0; ks < c.ksplit; ++ks) ss += c.ss_part[(size_t)ks * T + t];
+        for (int ks = 0; ks < c.ksplit; ++ks) ss += __ldcg(&c.ss_part[(size_t)ks * T + t]);
         r = prenorm_scale(ss, c.H);
         if (lane == 0) c.rnorm[t] = r;
       }
@@ -464,13 +504,14 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     for (int e = tid; e < E; e += 256) c.route_hist[(size_t)b * E + e] = cnt[0][e];
   }
   __syncthreads();
-  if (tid == 0 && !coop_grid_barrier(c.route_bar, (unsigned)G, c.status)) s_ok = 0;
+  if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
   __syncthreads();
   if (!s_ok) return;
 
   // ---------------------------------------------- phase 2: per-expert scan
+  // (many blocks only; up to kDirectBlocks, phase 3 sums the counts directly)
   const int per = (nb + 255) / 256;   // consecutive blocks per thread
-  for (int e = blockIdx.x; e < E; e += G) {
+  for (int e = blockIdx.x; !direct && e < E; e += G) {
     const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
     int loc = 0;
     for (int bb = b0; bb < b1; ++bb) loc += __ldcg(&c.route_hist[(size_t)bb * E + e]);
@@ -493,10 +534,21 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     if (tid == 255) c.route_hist[(size_t)nb * E + e] = before + incl;   // the expert's total
     __syncthreads();   // warp_tot reuse
   }
+  if (!direct) {
+    __syncthreads();
+    if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
+    __syncthreads();
+    if (!s_ok) return;
+  }
+  for (int e = tid; e < E; e += 256) {   // the experts' totals
+    int tot = 0;
+    if (direct)
+      for (int bb = 0; bb < nb; ++bb) tot += __ldcg(&c.route_hist[(size_t)bb * E + e]);
+    else
+      tot = __ldcg(&c.route_hist[(size_t)nb * E + e]);
+    s_tot[e] = tot;
+  }
   __syncthreads();
-  if (tid == 0 && !coop_grid_barrier(c.route_bar, (unsigned)G, c.status)) s_ok = 0;
-  __syncthreads();
-  if (!s_ok) return;
 
   // ---------------------------------------------- phase 3: offsets, scatter, x rows
   if (w == 0) {   // totals -> exclusive offsets (every CTA); CTA 0 publishes them and the active lists
@@ -504,7 +556,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     int n = 0, tiles = 0, base = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int ex = e0 + lane;
-      const int ce = ex < E ? __ldcg(&c.route_hist[(size_t)nb * E + ex]) : 0;
+      const int ce = ex < E ? s_tot[ex] : 0;
       int ci = ce;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -554,6 +606,14 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     const int p0 = b * 8 * k, p1 = min(T, b * 8 + 8) * k;
     const int nch = (p1 - p0 + 31) / 32;   // <= 8 (k <= 32)
     for (int i = tid; i < nch * E; i += 256) cnt[i / E][i % E] = 0;
+    for (int e = tid; e < E; e += 256) {   // the block's first row inside each expert's group
+      int base = 0;
+      if (direct)
+        for (int bb = 0; bb < b; ++bb) base += __ldcg(&c.route_hist[(size_t)bb * E + e]);
+      else
+        base = __ldcg(&c.route_hist[(size_t)b * E + e]);
+      s_base[e] = base;
+    }
     __syncthreads();
     int e = -1 - lane, rank = 0;
     const int p = p0 + w * 32 + lane;
@@ -567,7 +627,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     if (w < nch && p < p1) {
       int r = rank;
       for (int ch = 0; ch < w; ++ch) r += cnt[ch][e];
-      const int pos = s_off[e] + __ldcg(&c.route_hist[(size_t)b * E + e]) + r;
+      const int pos = s_off[e] + s_base[e] + r;
       c.sorted[pos] = p;
       c.p2r[p] = pos;
       s_pos[p - p0] = pos;
@@ -617,23 +677,20 @@ cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st) {
   FwdCtx cc = c;
   if (!gather) cc.xp = nullptr;
   cc.ksplit = (c.H + kRouteKC - 1) / kRouteKC;
-  const size_t lsmem = (size_t)2 * kRouteTile * (kRouteKC + 8) * sizeof(__half);
-  cudaError_t e = opt_in_smem((const void*)route_logits_mma_kernel, lsmem);
+  cudaError_t e = opt_in_smem((const void*)route_coop_kernel, kLogitSmem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;   // all CTAs of the cooperative launch must be co-resident
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel, 256, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel, 256, kLogitSmem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1 || c.num_sms < 1) return cudaErrorNotSupported;
-  // one grid size for every T (grid-stride loops over the blocks): the
-  // barrier counter stays a multiple of it from launch to launch
-  const int G = c.num_sms * (per_sm >= 2 ? 2 : 1);
-  const dim3 grid((c.T + kRouteTile - 1) / kRouteTile, (c.E + kRouteTile - 1) / kRouteTile, cc.ksplit);
-  e = launch_pdl(route_logits_mma_kernel, grid, dim3(128), lsmem, st, 1, cc);
-  if (e != cudaSuccess) return e;
+  // the grid size belongs to the barrier counter the kernel picks (fixed per
+  // counter); grid-stride loops cover any T
+  const int nb = (c.T + 7) / 8;
+  const int G = nb <= kDirectBlocks ? c.num_sms : c.num_sms * (per_sm >= 2 ? 2 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kLogitSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
