@@ -649,39 +649,25 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     if (p < P && __popc(peers & ((1u << lane) - 1u)) == 0) r_chunk[ch * E + e] = __popc(peers);
   }
   named_sync(6, (kNW - 1) * 32);
-  if (warp == 0) {   // counts, exclusive scan, active groups (ascending experts)
-    const int per = (E + 31) / 32;
-    int local[kMaxEPL];
-    int s = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i) {
-      const int e = lane * per + i;
-      local[i] = s;
-      if (i < per && e < E) {
-        int ce = 0;
-        for (int ch = 0; ch < nchunk; ++ch) ce += r_chunk[ch * E + e];
-        r_cnt[e] = ce;
-        s += ce;
-      }
-    }
-    int incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const int excl = incl - s;
-#pragma unroll
-    for (int i = 0; i < kMaxEPL; ++i) {
-      const int e = lane * per + i;
-      if (i < per && e < E) r_off[e] = excl + local[i];
-    }
-    if (lane == 31) r_off[E] = incl;
-    __syncwarp();
-    int n = 0;
+  if (warp == 0) {
+    // counts, exclusive scan and active groups (ascending experts) in one
+    // compact loop of 32-expert rounds: this runs once per launch on one warp,
+    // so its cost is mostly instruction fetch and grows with code size
+    int n = 0, base = 0;
+#pragma unroll 1
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int ce = e < E ? r_cnt[e] : 0;
+      int ce = 0;
+      if (e < E)
+        for (int ch = 0; ch < nchunk; ++ch) ce += r_chunk[ch * E + e];
+      int incl = ce;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int off = base + incl - ce;
+      if (e < E) r_off[e] = off;
       const int slot = ce > 0 ? r_table[e] : -1;
       const bool act = ce > 0 && slot >= 0;
       if (b == 0 && ce > 0 && slot < 0) {
@@ -691,11 +677,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       const unsigned am = __ballot_sync(kFull, act);
       const int pos = n + __popc(am & ((1u << lane) - 1u));
       if (act) {
-        r_astart[pos] = r_off[e];
+        r_astart[pos] = off;
         r_acount[pos] = ce;
       }
       n += __popc(am);
+      base += __shfl_sync(kFull, incl, 31);
     }
+    if (lane == 0) r_off[E] = base;
     if (lane == 0) r_misc[0] = n;
   }
   named_sync(6, (kNW - 1) * 32);
