@@ -450,6 +450,7 @@ DEV_INLINE void post_note(int* mbox, volatile int* head, volatile int* tail, int
 template <int GW>
 __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   constexpr int NG = kCW / GW;
+  constexpr int kMatUnroll = GW == 6 ? 2 : 1;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar;
   __shared__ int s_ok;
@@ -801,7 +802,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       }
       const int kc0 = wq * nkh / GW, kc1 = (wq + 1) * nkh / GW;   // the warp's K chunks
       float* rw = rg + wq * 2 * 16 * ntok;   // K-split partials -> rg[warp][mat][row][token]
-#pragma unroll
+      // up to 4-warp groups not unrolled: one copy of the MMA loop serves gate
+      // and up (a second copy doubles the instruction fetches); 6-warp groups
+      // (T > 8, two token tiles) measured faster unrolled
+#pragma unroll kMatUnroll
       for (int mat = 0; mat < 2; ++mat) {
         float acc[2][4];
 #pragma unroll
