@@ -532,9 +532,11 @@ def gpu_arm(args, rank, world, local_rank):
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4 weights x fp16 activations, fp32 accumulate", "data": "synthetic (seeded)",
+        "dtype": "f16", "data": "synthetic (seeded)",
         "config": workload_config(args, T) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                             "path": moe_w4a16.PATH_NAMES[path], "cuda_graph": True},
+                                             "path": moe_w4a16.PATH_NAMES[path], "cuda_graph": True,
+                                             "arithmetic": "int4 weights dequantised to f16 operands, "
+                                                           "f16 activations, f32 accumulation"},
         "roofline": roof, "layer_roofline": layer, "kernel_us": kern_us,
         "stage_event_us": [v * 1e3 for v in stage_avg],
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": wl.L * T * s.H * 2,
