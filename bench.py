@@ -415,16 +415,21 @@ def e2e_rate(wl, force, steps, world, local_rank):
         xh = [[wl.xs[l][r].cpu().pin_memory() for r in range(ROTATE)] for l in range(wl.L)]
     oh = [torch.empty(T, H, dtype=torch.float16).pin_memory() for _ in range(2 if wl.chain else wl.L)]
 
+    # independent layers alternate over two streams, so one layer's copies
+    # overlap another layer's kernels; a chained stack stays on one stream
+    # (stream order carries a layer's host output into the next layer's input)
+    streams = [torch.cuda.current_stream()] if wl.chain else [torch.cuda.Stream(), torch.cuda.Stream()]
+
     def one(i):
-        # every layer's H2D copy, forward and D2H copy enqueued on one stream
-        # (stream order chains a layer's host output into the next layer's
-        # input), then one synchronisation: the step's outputs are on the host
+        # every layer's H2D copy, forward and D2H copy enqueued, then one
+        # synchronisation: the step's outputs are on the host
         for l, m in enumerate(wl.layers):
             if wl.chain:
                 src = xh[i % ROTATE] if l == 0 else oh[(l - 1) % 2]
                 m.forward_host_async(src, wl.rws[l], oh[l % 2], wl.biases[l], wl.flags | force)
             else:
-                m.forward_host_async(xh[l][i % ROTATE], wl.rws[l], oh[l], wl.biases[l], wl.flags | force)
+                m.forward_host_async(xh[l][i % ROTATE], wl.rws[l], oh[l], wl.biases[l], wl.flags | force,
+                                     stream=streams[l % 2])
         torch.cuda.synchronize()
 
     for i in range(2):
