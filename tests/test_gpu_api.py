@@ -126,6 +126,37 @@ def test_forward_host_matches_forward(tiny):
     assert np.array_equal(out, oh.astype(np.float64))
 
 
+def test_forward_host_async_two_streams():
+    """Two handles (OLMoE-shaped decode layers, single-launch cooperative
+    kernel) enqueued alternately on two streams with host buffers, as the
+    benchmark's end-to-end leg does: outputs equal the device forwards and no
+    bounded wait gave up."""
+    import torch
+    layers = [synth.olmoe_decode_layer(), synth.tiny_layer()]
+    T = 4
+    ms = [gp.make_handle(layer, 16) for layer in layers]
+    try:
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        xs = [[synth.draw_x(60 + 10 * j + r, T, layer.shape.hidden) for r in range(3)]
+              for j, layer in enumerate(layers)]
+        rws = [gp.to_dev(layer.router_w) for layer in layers]
+        outs = [[torch.empty(T, layer.shape.hidden, dtype=torch.float16).pin_memory() for _ in range(3)]
+                for layer in layers]
+        xh = [[torch.from_numpy(x).pin_memory() for x in row] for row in xs]
+        for r in range(3):
+            for j, m in enumerate(ms):
+                m.forward_host_async(xh[j][r], rws[j], outs[j][r], None, 0, stream=streams[j])
+        torch.cuda.synchronize()
+        for j, (m, layer) in enumerate(zip(ms, layers)):
+            for r in range(3):
+                ref, _ = gp.gpu_forward(m, layer, xs[j][r], 0)
+                assert np.array_equal(outs[j][r].numpy().astype(np.float64), ref)
+            assert m.get_status() == (F.OK, 0)
+    finally:
+        for m in ms:
+            m.close()
+
+
 def test_forward_host_async_chain_matches_forward(tiny):
     """Three enqueued host-buffer forwards on one handle and one stream, each
     reading the previous one's host output (stream order), then one
