@@ -25,7 +25,7 @@ def qwen():
     return synth.qwen_partial_layer()
 
 
-@pytest.mark.parametrize("T", [4, 1, 3, 13, 37, 64, 100, 257])
+@pytest.mark.parametrize("T", [4, 1, 3, 8, 9, 13, 37, 64, 100, 257])
 @pytest.mark.parametrize("force", [0, F.FORCE_GEMV | F.UNFUSED, F.FORCE_GEMM])
 def test_tiny(tiny, T, force):
     x = synth.draw_x(synth.SEED_TINY, T, tiny.shape.hidden)
