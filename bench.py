@@ -340,6 +340,24 @@ class Workload:
             m.close()
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the whole job is as slow as its
+    slowest replica); the value itself on one rank.  `device`: where the
+    reduction tensor lives (the rank's GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (weak scaling: each rank runs the same work)."""
+    return units_per_rank * world / seconds
+
+
 def time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks):
     import torch
     for i in range(warm):
@@ -368,11 +386,7 @@ def time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=torch.device("cuda", local_rank))
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, torch.device("cuda", local_rank))
     return ms, clk.summary(peaks.get("sm_max_mhz"))
 
 
@@ -439,12 +453,8 @@ def e2e_rate(wl, force, steps, world, local_rank):
     t0 = time.perf_counter()
     for i in range(steps):
         one(i)
-    el = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([el], device=torch.device("cuda", local_rank))
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        el = float(t.item())
-    return wl.L * T * steps * world / el
+    el = max_over_ranks(time.perf_counter() - t0, world, torch.device("cuda", local_rank))
+    return job_rate(wl.L * T * steps, world, el)
 
 
 def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
@@ -527,7 +537,7 @@ def gpu_arm(args, rank, world, local_rank):
     ms, clocks = time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks)
     path, launches = wl.layers[0].last_path()
     assert all(m.last_path() == (path, launches) for m in wl.layers)
-    value = wl.L * T * steps * world / (ms / 1e3)
+    value = job_rate(wl.L * T * steps, world, ms / 1e3)
     stage_avg = stage_times(wl, force, stream)
     layer_ms = ms / (steps * wl.L)
     roof, layer, kern_us, sha = roofline(wl, path, layer_ms, stage_avg, avg_u, peaks)
@@ -580,7 +590,7 @@ def stack_sweep(args, rank, world, local_rank):
             steps = args.steps or max(5, min(400, 4096 // T))
             ms, clocks = time_graphs(wl, force, steps, 3, stream, world, local_rank, peaks)
             path, _ = wl.layers[0].last_path()
-            row[fam] = {"tokens_per_s_per_layer": T * steps * world / (ms / 1e3),
+            row[fam] = {"tokens_per_s_per_layer": job_rate(T * steps, world, ms / 1e3),
                         "us_per_layer": ms * 1e3 / (steps * wl.L), "path": moe_w4a16.PATH_NAMES[path],
                         "sm_mhz": clocks["sm_mhz"], "reasons": clocks["reasons"]}
         for m in wl.layers:
@@ -638,12 +648,14 @@ def cache_bench(args, rank, world, local_rank):
     for i in range(max(3, args.warmup)):
         one(i)
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     s0 = cache.stats()
     t0 = time.perf_counter()
     for i in range(steps):
         one(i)
     torch.cuda.synchronize()
-    el = time.perf_counter() - t0
+    el = max_over_ranks(time.perf_counter() - t0, world, torch.device("cuda", local_rank))
     s1 = cache.stats()
     st, miss = m.get_status()
     assert st == M.OK and miss == 0, (st, miss)
@@ -656,7 +668,7 @@ def cache_bench(args, rank, world, local_rank):
     cfg["layers_per_step"] = 1
     cfg["l2"] = "misses copied from host memory; resident weights 171 MB"
     res = {"metric": "MoE-layer tokens/s with the expert cache's miss path in the loop",
-           "value": T * steps * world / el, "unit": UNIT, "n_gpus": world, "steps": steps,
+           "value": job_rate(T * steps, world, el), "unit": UNIT, "n_gpus": world, "steps": steps,
            "ms_per_step": el * 1e3 / steps, "higher_is_better": True,
            "config": cfg | {"path": "route + acquire + forward + release per step",
                                                 "published_rows": s.slots, "spare_rows": group,
