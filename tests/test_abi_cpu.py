@@ -76,6 +76,8 @@ def test_null_handle_calls(lib):
     assert lib.moe_w4a16_get_status(None, None) == moe_w4a16.ERR_INVALID_ARG
     assert lib.moe_w4a16_slot_bytes(None) == 0
     assert lib.moe_w4a16_offload_enable(None, 4) == moe_w4a16.ERR_INVALID_ARG
+    assert lib.moe_w4a16_forward_host(None, None, 0, None, None, 0, None, None) == moe_w4a16.ERR_INVALID_ARG
+    assert lib.moe_w4a16_forward_host_async(None, None, 0, None, None, 0, None, None) == moe_w4a16.ERR_INVALID_ARG
 
 
 def test_no_device_is_a_cuda_error(lib):
