@@ -42,7 +42,11 @@
  * and is counted as a miss (see moe_w4a16_get_status).
  *
  * Threading: a handle is not thread-safe; calls on one handle must be
- * serialised by the caller.  Asynchrony: every call taking a cudaStream_t
+ * serialised by the caller.  Forwards of one handle share its workspaces and
+ * counters: enqueue them on one stream (or order them with events).  Different
+ * handles may run on different streams at the same time, the single-launch
+ * cooperative kernels included (each handle has its own counters).
+ * Asynchrony: every call taking a cudaStream_t
  * only enqueues work on that stream (after synchronous argument checks);
  * device buffers passed in must stay valid until the stream reaches the call.
  * forward enqueues no allocation, no host synchronisation and no
