@@ -37,9 +37,13 @@
  *   y_j   = W_d (SiLU(W_g xin) * (W_u xin))   for expert ids_j
  *   out   = (RESIDUAL ? x : 0) + sum_{j=0..k-1} w_j y_j        (FP32, j order)
  * rounded to FP16 at two points: the SiLU*up product h (the A16 operand of the
- * down projection) and the final out.  Dequantised weights are formed as the
- * FP16 value nearest q*s.  A routed expert whose slot is absent contributes 0
- * and is counted as a miss (see moe_w4a16_get_status).
+ * down projection) and the final out; the grouped-GEMM path also rounds each
+ * expert output y_j to FP16 before the FP32 combine.  How q*s enters the
+ * multiply depends on the kernel family: the single-launch decode kernel
+ * multiplies the exact integers q and applies s to each 64-wide partial sum
+ * in FP32 (q*s exact); the separate-launch decode kernels and the grouped
+ * GEMM multiply the FP16 value nearest q*s.  A routed expert whose slot is
+ * absent contributes 0 and is counted as a miss (see moe_w4a16_get_status).
  *
  * Threading: a handle is not thread-safe; calls on one handle must be
  * serialised by the caller.  Forwards of one handle share its workspaces and
@@ -196,9 +200,13 @@ MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
 #define MOE_W4A16_NOALLOC_MAX_LOGITS 786432   /* T * num_experts * ceil(hidden / 256) */
 #define MOE_W4A16_NOALLOC_MAX_PAIRS 65536     /* T * top_k */
 
-/* Routing of one layer (router logits, softmax / top-k, stable permutation:
- * the same kernels and results as the routing part of moe_w4a16_forward for
- * T > 64) that allocates nothing and needs no handle.  The Horizon RunMap
+/* Routing of one layer (router logits, softmax / top-k, stable permutation)
+ * that allocates nothing and needs no handle.  It runs four launches
+ * (tensor-core logits tiles over 256-wide K slices, top-k summing the slices
+ * in order, per-expert scan, stable scatter); its ids, weights and
+ * permutation equal bit for bit those of moe_w4a16_forward's cooperative
+ * router (the forward's router above 8 tokens, outside the single-launch
+ * decode kernel), which sums the same logits tiles in the same order.  The Horizon RunMap
  * pages have no counterpart to this entry point; it exists for callers that
  * cannot call cudaMalloc: code that runs inside a runtime whose allocator
  * already owns all device memory (plugins of serving engines that hand out
@@ -214,7 +222,10 @@ MOE_W4A16_API const char* moe_w4a16_last_error(const moe_w4a16_handle* h);
  * Scratch lives in one file-scope device array of 5 MiB that every device
  * which loads the library keeps until the process exits.  The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture on the device.
+ * caches it for the life of the process; make that first call before any
+ * stream capture on the device, and do not reset the device
+ * (cudaDeviceReset) while the library is loaded: the cached address would
+ * then point into a context that no longer exists.
  * Limits: T <= MOE_W4A16_NOALLOC_MAX_TOKENS, T*E*ceil(H/256) <=
  * ..._MAX_LOGITS, T*k <= ..._MAX_PAIRS, E <= 256, k <= min(E, 32), H a
  * multiple of 64 and <= ..._MAX_HIDDEN;

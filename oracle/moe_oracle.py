@@ -42,6 +42,7 @@ import numpy as np
 
 BLOCK = 256          # K values per FP16 scale
 NEAR_TIE_GAP = 1e-4  # logit gap below which a routing decision is flagged
+FP16_MAX = 65504.0   # largest finite IEEE binary16 value
 
 
 # ------------------------------------------------------------------ format
@@ -187,6 +188,7 @@ class LayerResult:
     weights: np.ndarray         # [T, k]
     perm: Permutation
     near_tie: np.ndarray        # [T] bool
+    overflow: np.ndarray        # [T, H] bool: |out| > FP16_MAX (an FP16 output is +-inf there)
     y: Optional[np.ndarray] = None   # [P, H] per-pair expert outputs (pair order)
 
 
@@ -199,6 +201,8 @@ def moe_layer(x, router_w, bias, experts, k: int, flags: int = 0,
     = identity).  A routed expert without a slot contributes 0.
     out[t] = (x[t] if RESIDUAL) + sum_j w[t, j] * y[t*k + j] summed in j order.
     With PRENORM the router and experts see x / rms(x); the residual stays x.
+    overflow flags the outputs whose magnitude is beyond the largest finite
+    FP16 value, where an FP16 result rounds to +-inf.
     """
     gq, gs, uq, us, dq, ds = experts
     x0 = np.asarray(x, np.float64)
@@ -223,11 +227,5 @@ def moe_layer(x, router_w, bias, experts, k: int, flags: int = 0,
     for j in range(k):
         out += w[:, j:j + 1] * y[np.arange(T) * k + j]
     return LayerResult(out, logits, ids, w, perm, near_tie_flags(logits, k),
-                       y if keep_y else None)
+                       np.abs(out) > FP16_MAX, y if keep_y else None)
 
-
-def moe_token(x_t, router_w, bias, experts, k: int, flags: int = 0, expert_to_slot=None) -> np.ndarray:
-    """One token's output row computed on its own (for sampled checks at full
-    size): same definition as moe_layer restricted to a single token."""
-    return moe_layer(np.asarray(x_t)[None, :], router_w, bias, experts, k, flags,
-                     expert_to_slot).out[0]

@@ -146,6 +146,21 @@ def pin_residual_prenorm(o):
     assert np.allclose(r2.out, 4.0 + s4, rtol=0, atol=1e-12)
 
 
+def pin_overflow(o):
+    """Example A with down q = +-7 at scale 65504 (0x7BFF, the largest finite
+    FP16 value): y = +-7 * 65504 * SiLU(1) = +-335,208.6..., beyond FP16 range
+    on both signs; example A itself (out = SiLU(1)) is flagged nowhere."""
+    g = load_golden("example_a.json")
+    for byte, sign in ((0x07, 1.0), (0x09, -1.0)):
+        ex = list(stack_experts(example_expert(0x11, 0x11, byte)))
+        ex[5] = np.full_like(ex[5], 0x7BFF)
+        r = _run_example(o, tuple(ex), None, 1)
+        assert np.allclose(r.out, sign * 7.0 * 65504.0 * g["expected_out_every_h"], rtol=1e-14, atol=0)
+        assert r.overflow.shape == r.out.shape and r.overflow.all()
+    ok = _run_example(o, stack_experts(example_expert(0x11, 0x11, 0x02)), None, 1)
+    assert not ok.overflow.any()
+
+
 # ------------------------------------------------------- routing specifics
 
 def pin_router_rules(o):
@@ -332,7 +347,7 @@ def pin_invariants(o):
 
 ALL_PINS = [pin_nibble_table, pin_pack_examples, pin_block_scales, pin_example_a, pin_example_b,
             pin_example_c, pin_residual_prenorm, pin_router_rules, pin_near_tie, pin_permutation,
-            pin_brute_force, pin_brute_force_slots, pin_closed_forms, pin_invariants]
+            pin_brute_force, pin_brute_force_slots, pin_closed_forms, pin_invariants, pin_overflow]
 
 
 def failing_pins(o):

@@ -33,11 +33,20 @@ def test_tiny(tiny, T, force):
     print(f"tiny T={T} rel={err:.2e} flagged={nflag}")
 
 
+@pytest.mark.parametrize("T", [12, 20])
 @pytest.mark.parametrize("flags", [F.RESIDUAL, F.PRENORM, F.RESIDUAL | F.PRENORM])
 @pytest.mark.parametrize("force", [0, F.FORCE_GEMV | F.UNFUSED, F.FORCE_GEMM])
-def test_tiny_flags(tiny, flags, force):
-    x = synth.draw_x(synth.SEED_TINY, 20, tiny.shape.hidden)
-    gp.check_full(tiny, x, flags=flags | force, max_tokens=32)
+def test_tiny_flags(tiny, flags, force, T):
+    """T = 12 with force = 0 runs the single-launch decode kernel; T = 20 the
+    separate-launch decode path."""
+    x = synth.draw_x(synth.SEED_TINY, T, tiny.shape.hidden)
+    m = gp.make_handle(tiny, 32)
+    try:
+        gp.check_full(tiny, x, flags=flags | force, m=m)
+        if force == 0:
+            assert m.last_path()[0] == (F.PATH_DECODE_FUSED if T <= 16 else F.PATH_DECODE)
+    finally:
+        m.close()
 
 
 def test_tiny_gemm_large_groups():
@@ -54,6 +63,23 @@ def test_olmoe_decode(olmoe, T, force):
     x = synth.draw_x(synth.SEED_OLMOE_DECODE, T, olmoe.shape.hidden)
     err, nflag = gp.check_full(olmoe, x, flags=force, max_tokens=2048)
     print(f"olmoe T={T} rel={err:.2e} flagged={nflag}")
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+@pytest.mark.parametrize("flags", [F.PRENORM, F.RESIDUAL | F.PRENORM])
+def test_olmoe_decode_prenorm_fused(olmoe, T, flags):
+    """PRENORM on the single-launch decode kernel with real routing: 1/rms is
+    folded into the router logits (it can change the top-k) and into the
+    gate/up epilogue."""
+    x = synth.draw_x(synth.SEED_OLMOE_DECODE + 50, T, olmoe.shape.hidden)
+    x = (x.astype(np.float32) * np.float32(3.0)).astype(np.float16)   # rms far from 1
+    m = gp.make_handle(olmoe, 16)
+    try:
+        err, nflag = gp.check_full(olmoe, x, flags=flags, m=m)
+        assert m.last_path() == (F.PATH_DECODE_FUSED, 1)
+    finally:
+        m.close()
+    print(f"olmoe prenorm T={T} flags={flags} rel={err:.2e} flagged={nflag}")
 
 
 @pytest.mark.parametrize("T", [1, 8, 32])
@@ -75,3 +101,24 @@ def test_olmoe_prefill_sampled(variant, force):
     rows = np.concatenate([rows, [0, T - 1]])
     err, nflag = gp.check_sampled(layer, x, rows, flags=force)
     print(f"prefill v{variant} sampled rel={err:.2e} flagged={nflag}")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_olmoe_prefill_every_row(variant):
+    """T = 2048 prefill, every output row against the oracle (grouped-GEMM
+    path, and the decode kernels forced), one oracle evaluation for both."""
+    layer = synth.olmoe_prefill_layer(variant)
+    seed = synth.SEED_OLMOE_PREFILL if variant == 1 else synth.SEED_OLMOE_PREFILL_SKEW
+    x = synth.draw_x(seed, 2048, layer.shape.hidden)
+    m = gp.make_handle(layer, 2048)
+    try:
+        got = [gp.gpu_forward(m, layer, x, force) for force in (0, F.FORCE_GEMV)]
+        assert m.get_status() == (F.OK, 0)
+    finally:
+        m.close()
+    ref = gp.oracle_layer(layer, x, 0)
+    assert not ref.overflow.any()
+    for out, dbg in got:
+        gp.assert_routing(dbg, ref.ids, ref.weights, ref.near_tie, layer.shape.num_experts, ref.perm)
+        err = gp.assert_output(out, ref.out, ~ref.near_tie)
+        print(f"prefill v{variant} every row rel={err:.2e} flagged={int(ref.near_tie.sum())}")

@@ -236,15 +236,6 @@ DEV_INLINE uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// TMA: four rows (r0..r3) x box columns at column c0 of a 2-D tensor map.
-DEV_INLINE void tma_gather4(void* dst, const void* tmap, int c0, int r0, int r1, int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA: one box at (c0, r0) of a 2-D tensor map.
 DEV_INLINE void tma_load_2d(void* dst, const void* tmap, int c0, int r0, uint64_t* bar) {
   asm volatile(
