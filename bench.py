@@ -19,7 +19,12 @@ Workloads (--workload):
            T tokens; --sweep times T in {1, 8, 64, 512, 2048} with the decode
            kernels and the grouped GEMM forced in turn and reports the
            crossover.
-Metric: MoE-layer tokens/s = layers * T * steps / time.
+Metric: MoE-layer tokens/s = layers * T * steps / time.  The default decode
+line also carries "prefill": the OLMoE prefill layers (T = 2048, both
+variants) timed in the same run, with their TFLOP/s against the measured
+FP16/BF16 dense peak.  Every timed region records one event pair per CUDA
+graph replay (median, min, max) and samples the SM clock and clock-event
+reasons through NVML every 2 ms.
 
 Prints ONE JSON line (rank 0).  --impl reference times the float64 CPU oracle
 on the same workload instead (bounded sample, host cores).
@@ -77,6 +82,8 @@ def parse():
     ap.add_argument("--cache", action="store_true",
                     help="qwen: partial residency through the expert cache (misses copied from host memory)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode: skip the OLMoE prefill legs (T = 2048, both variants) timed after the decode line")
     ap.add_argument("--layers", type=int, default=None, help="layers (pools) per step")
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help=argparse.SUPPRESS)
@@ -175,7 +182,126 @@ def cpu_sample_text(args, leg):
             f"in {leg['seconds']:.1f} s, 1 thread")
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(args):
+    """The oracle as it stands on the host cores: one process with one BLAS
+    thread, then one such process per core at once (each on its own rotating
+    batches: token-parallel work, since tokens are independent); the
+    all-cores rate is the sum of the processes' rates."""
+    import concurrent.futures
+    single = run_cpu_leg(args, seconds=args.cpu_seconds)
+    n = os.cpu_count() or 1
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        legs = list(ex.map(lambda _: run_cpu_leg(args, seconds=args.cpu_seconds), range(n)))
+    total = sum(l["value"] for l in legs)
+    steps = sum(l["steps"] for l in legs)
+    return {"value": total, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": (f"{n} processes at once (one per host core, 1 BLAS thread each), {steps} float64-oracle "
+                       f"forwards of one {shape_of(args).name}-shaped layer at T={tokens_of(args)} in "
+                       f"{max(l['seconds'] for l in legs):.1f} s; rate = sum of the processes' rates"),
+            "single_thread": {"value": single["value"], "cores": 1, "sample": cpu_sample_text(args, single)},
+            "nproc": n, "cpu_model": cpu_model()}
+
+
 # ------------------------------------------------------------------ clocks
+
+REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only
+    queries) from a thread every ~2 ms while the timed region runs, so even
+    a region of a few milliseconds gets several samples.  Falls back to
+    nvidia-smi (100 ms period) when the NVML library cannot be loaded."""
+
+    def __init__(self, local_rank, period_s=0.002):
+        self.local_rank, self.period = local_rank, period_s
+        self.samples, self.source = [], None
+        self.nvml = self.dev = None
+        self._smi = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            dev = ctypes.c_void_p()
+            found = False
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(local_rank)
+                bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+                found = nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(dev)) == 0
+            except Exception:   # noqa: BLE001 - older torch: no PCI ids
+                found = False
+            if not found and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(local_rank), ctypes.byref(dev)) != 0:
+                raise OSError("no NVML handle")
+            self.nvml, self.dev = nv, dev
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(dev, ctypes.c_int(1), ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            self.source = "nvml"
+        except OSError:
+            self.source = "nvidia-smi"
+
+    def _read(self):
+        import ctypes
+        nv, dev = self.nvml, self.dev
+        clk, mw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        nv.nvmlDeviceGetClockInfo(dev, ctypes.c_int(1), ctypes.byref(clk))   # NVML_CLOCK_SM
+        nv.nvmlDeviceGetPowerUsage(dev, ctypes.byref(mw))
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(dev, ctypes.byref(rs))
+        return float(clk.value), mw.value / 1000.0, int(rs.value)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._read())
+            except Exception:   # noqa: BLE001 - a failed query ends sampling
+                return
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        import threading
+        if self.nvml is not None:
+            self._stop = threading.Event()
+            self.samples = [self._read()]
+            self._thr = threading.Thread(target=self._loop, daemon=True)
+            self._thr.start()
+        else:
+            self._smi = ClockSampler(self.local_rank).__enter__()
+        return self
+
+    def __exit__(self, *exc):
+        if self.nvml is not None:
+            self._stop.set()
+            self._thr.join()
+            self.samples.append(self._read())
+        else:
+            self._smi.__exit__(*exc)
+
+    def summary(self, max_mhz_fallback):
+        if self.nvml is None:
+            return self._smi.summary(max_mhz_fallback) | {"source": "nvidia-smi"}
+        sm = [c for c, _, _ in self.samples]
+        reasons = sorted({n for _, _, r in self.samples for n, b in REASON_BITS.items() if r & b})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(p for _, p, _ in self.samples), "reasons": reasons,
+                "samples": len(sm), "source": "nvml, 2 ms period"}
+
 
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -376,18 +502,22 @@ def time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
+    # one event before every replay and one after the last: the timed region
+    # is first to last, each replay's own duration the gap between neighbours
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with NvmlSampler(local_rank) as clk:
         with torch.cuda.stream(stream):
-            ev0.record(stream)
             for i in range(steps):
+                evs[i].record(stream)
                 graphs[i % ROTATE].replay()
-            ev1.record(stream)
+            evs[steps].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, torch.device("cuda", local_rank))
-    return ms, clk.summary(peaks.get("sm_max_mhz"))
+    ms = max_over_ranks(evs[0].elapsed_time(evs[steps]), world, torch.device("cuda", local_rank))
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    stats = {"n": steps, "median_ms": statistics.median(per), "min_ms": per[0], "max_ms": per[-1]}
+    return ms, clk.summary(peaks.get("sm_max_mhz")), stats
 
 
 def stage_times(wl, force, stream):
@@ -511,6 +641,50 @@ def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
     return roof, layer, {n: v[0] * 1e3 for n, v in kern.items()}, sha
 
 
+def prefill_legs(args, dev, local_rank, world, peaks, stream, steps=60):
+    """OLMoE-shaped prefill (T = 2048), both variants, timed in the same run as
+    the decode line: 16 layers per step, one CUDA-graph replay per step."""
+    import torch
+    from w4a16_compact_expert_gb300 import moe_w4a16 as M
+    res = {}
+    sus = peaks.get("bf16_tflops_sustained") or 1700.0
+    burst = peaks.get("bf16_tflops") or 1900.0
+    for variant in (1, 2):
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.variant, a.tokens = "prefill", variant, 2048
+        T = 2048
+        wl = Workload(a, T, dev, local_rank)
+        ms, clocks, replay = time_graphs(wl, 0, steps, 3, stream, world, local_rank, peaks)
+        path, launches = wl.layers[0].last_path()
+        stage_avg = stage_times(wl, 0, stream)
+        for m in wl.layers:
+            st, miss = m.get_status()
+            assert st == M.OK and miss == 0, (st, miss)
+        s = wl.shape
+        P = T * s.k
+        layer_s = ms / 1e3 / (steps * wl.L)
+        flops = 2.0 * P * 3 * s.H * s.I + 2.0 * T * s.E * s.H
+        gu_s = stage_avg[1] / 1e3
+        gu_tf = 2.0 * P * 2 * s.H * s.I / gu_s / 1e12
+        tf = flops / layer_s / 1e12
+        res[f"variant{variant}"] = {
+            "workload": workload_config(a, T)["workload"], "path": M.PATH_NAMES[path],
+            "launches_per_layer_forward": launches, "steps": steps, "tokens_per_s": job_rate(wl.L * T * steps,
+                                                                                              world, ms / 1e3),
+            "us_per_layer": layer_s * 1e6, "algorithmic_flops_per_layer": flops, "tflops": tf,
+            "frac_sustained": tf / sus, "frac_burst": tf / burst,
+            "gemm_gate_up_us": stage_avg[1] * 1e3, "gemm_gate_up_tflops": gu_tf,
+            "gemm_gate_up_frac_sustained": gu_tf / sus, "gemm_down_us": stage_avg[2] * 1e3,
+            "route_gather_us": stage_avg[0] * 1e3, "combine_us": stage_avg[3] * 1e3,
+            "step_replays": replay, "clocks": clocks,
+            "peaks": {"sustained_tflops": sus, "burst_tflops": burst,
+                      "source": "measured bf16 (fp16 nominal = bf16)"}}
+        wl.close()
+        del wl
+        torch.cuda.empty_cache()
+    return res
+
+
 def force_flag(name):
     from w4a16_compact_expert_gb300 import moe_w4a16 as M
     return {"auto": 0, "gemv": M.FORCE_GEMV, "unfused": M.FORCE_GEMV | M.UNFUSED, "gemm": M.FORCE_GEMM,
@@ -534,7 +708,7 @@ def gpu_arm(args, rank, world, local_rank):
         st, miss = m.get_status()
         assert st == moe_w4a16.OK and miss == 0, (st, miss)
     stream = torch.cuda.Stream(device=dev)
-    ms, clocks = time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks)
+    ms, clocks, replay = time_graphs(wl, force, steps, warm, stream, world, local_rank, peaks)
     path, launches = wl.layers[0].last_path()
     assert all(m.last_path() == (path, launches) for m in wl.layers)
     value = job_rate(wl.L * T * steps, world, ms / 1e3)
@@ -558,7 +732,15 @@ def gpu_arm(args, rank, world, local_rank):
                 "d2h_bytes_per_step": wl.L * T * s.H * 2, "steps": e2e_steps},
         "gpu_launches": steps * wl.L * launches, "launches_per_layer_forward": launches,
         "clocks": clocks, "kernel_src": sha,
+        "step_replays": replay | {"note": "one CUDA-graph replay = one step (every layer once); per-replay "
+                                          "durations from an event pair around each replay"},
     }
+    if args.workload == "decode" and args.force == "auto" and not args.tokens and not args.no_prefill:
+        wl.close()
+        del wl
+        torch.cuda.empty_cache()
+        res["prefill"] = prefill_legs(args, dev, local_rank, world, peaks, stream)
+        return res
     if path == moe_w4a16.PATH_OFFLOAD:
         # what the expansion moves per layer, next to the compact path's weight bytes
         exp_bytes = avg_u * 3 * s.I * s.H * 2
@@ -588,7 +770,7 @@ def stack_sweep(args, rank, world, local_rank):
         for fam in ("gemv", "gemm"):
             force = force_flag(fam)
             steps = args.steps or max(5, min(400, 4096 // T))
-            ms, clocks = time_graphs(wl, force, steps, 3, stream, world, local_rank, peaks)
+            ms, clocks, _ = time_graphs(wl, force, steps, 3, stream, world, local_rank, peaks)
             path, _ = wl.layers[0].last_path()
             row[fam] = {"tokens_per_s_per_layer": job_rate(T * steps, world, ms / 1e3),
                         "us_per_layer": ms * 1e3 / (steps * wl.L), "path": moe_w4a16.PATH_NAMES[path],
@@ -716,9 +898,7 @@ def main():
         # CPU baseline first, in its own process, before this process touches the GPU.
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            leg = run_cpu_leg(args, seconds=args.cpu_seconds)
-            cpu = {"value": leg["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": cpu_sample_text(args, leg)}
+            cpu = cpu_baseline(args)
         res = gpu_arm(args, rank, world, local_rank)
         res["cpu_baseline"] = cpu
     if rank == 0:
