@@ -450,14 +450,20 @@ class Workload:
             m.forward(x, self.rws[l], self.biases[l], self.flags | force, out=out)
 
     def unique_experts(self, force):
-        """Mean number of distinct routed experts per layer forward (from the actual routing)."""
+        """Mean number of distinct routed experts per layer forward (from the
+        actual routing); also keeps layer 0's count for each activation batch
+        (self.u_layer0, in launch order: the batches r = 0 .. ROTATE - 1)."""
         import torch
         n = []
+        self.u_layer0 = []
         for r in range(ROTATE):
             for l, m in enumerate(self.layers):
                 x, out = self._io(l, r)
                 _, dbg = m.forward(x, self.rws[l], self.biases[l], self.flags | force, out=out, debug=True)
-                n.append(int(torch.unique(dbg["ids"]).numel()))
+                u = int(torch.unique(dbg["ids"]).numel())
+                n.append(u)
+                if l == 0:
+                    self.u_layer0.append(u)
         torch.cuda.synchronize()
         return statistics.mean(n)
 
@@ -634,7 +640,11 @@ def roofline(wl, path, layer_ms, stage_avg, avg_u, peaks):
     roof = {"bound": "tensor" if tensor else "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
             "unit": unit, "frac": achieved / peak, "peak_source": src, "avg_launch_us": dom_ms * 1e3,
             "traffic": profiled_traffic(dom, T, sha)} | work
+    per_batch = [u * (s.gate_up_bytes + s.down_bytes) + (layer_bytes - avg_u * (s.gate_up_bytes + s.down_bytes))
+                 for u in getattr(wl, "u_layer0", [])]
     layer = {"algorithmic_bytes_per_layer": layer_bytes, "us_per_layer": layer_ms * 1e3,
+             "layer0_unique_experts_per_batch": getattr(wl, "u_layer0", []),
+             "layer0_algorithmic_bytes_per_batch": per_batch,
              "achieved_gbs": layer_bytes / (layer_ms / 1e3) / 1e9,
              "hbm_frac": layer_bytes / (layer_ms / 1e3) / 1e9 / hbm,
              "achieved_tflops": layer_flops / (layer_ms / 1e3) / 1e12, "avg_unique_experts": avg_u}
