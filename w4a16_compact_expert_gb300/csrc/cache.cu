@@ -13,9 +13,13 @@
 // simulation, which moves no bytes and whose lease events complete only when
 // a test says so.
 #include <algorithm>
+#include <atomic>
+#include <condition_variable>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "handle.h"
@@ -39,6 +43,112 @@ struct Retiring {
 };
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Host threads that copy a miss's canonical arrays from the backing into its
+// pinned staging entry together: one host thread's copy rate (about 14 GB/s
+// on the GB300's Grace host) would bound the whole miss path, well below
+// what the host-to-device link carries.  The calling thread takes part; the
+// bytes are cut into chunks that the threads claim from one counter.
+class CopyPool {
+ public:
+  struct Seg {
+    uint8_t* dst;
+    const uint8_t* src;
+    size_t bytes;
+  };
+
+  explicit CopyPool(int workers) {
+    for (int i = 0; i < workers; ++i) th_.emplace_back([this] { loop(); });
+  }
+  ~CopyPool() {
+    {
+      std::lock_guard<std::mutex> lk(mu_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : th_) t.join();
+  }
+  int threads() const { return (int)th_.size() + 1; }
+
+  // Copies every segment; returns when all bytes are in place.
+  void copy(const std::vector<Seg>& segs) {
+    size_t total = 0;
+    for (const Seg& sg : segs) total += sg.bytes;
+    if (th_.empty() || total < 2 * kChunk) {
+      for (const Seg& sg : segs) std::memcpy(sg.dst, sg.src, sg.bytes);
+      return;
+    }
+    {
+      std::lock_guard<std::mutex> lk(mu_);
+      segs_ = &segs;
+      nchunks_ = 0;
+      for (const Seg& sg : segs) nchunks_ += (sg.bytes + kChunk - 1) / kChunk;
+      next_.store(0);
+      done_ = 0;
+      ++job_;
+    }
+    cv_.notify_all();
+    const size_t mine = work();
+    std::unique_lock<std::mutex> lk(mu_);
+    done_ += mine;
+    done_cv_.wait(lk, [this] { return done_ == nchunks_; });
+    segs_ = nullptr;
+  }
+
+ private:
+  static constexpr size_t kChunk = 256 * 1024;
+
+  // Claims chunks until none is left; returns how many this thread copied.
+  size_t work() {
+    size_t n = 0;
+    for (;;) {
+      size_t i = next_.fetch_add(1);
+      if (i >= nchunks_) return n;
+      for (const Seg& sg : *segs_) {   // chunk i -> (segment, offset)
+        const size_t cs = (sg.bytes + kChunk - 1) / kChunk;
+        if (i < cs) {
+          const size_t off = i * kChunk, len = std::min(kChunk, sg.bytes - off);
+          std::memcpy(sg.dst + off, sg.src + off, len);
+          break;
+        }
+        i -= cs;
+      }
+      ++n;
+    }
+  }
+
+  void loop() {
+    uint64_t seen = 0;
+    for (;;) {
+      {
+        std::unique_lock<std::mutex> lk(mu_);
+        cv_.wait(lk, [&] { return stop_ || job_ != seen; });
+        if (stop_) return;
+        seen = job_;
+      }
+      const size_t mine = work();
+      std::lock_guard<std::mutex> lk(mu_);
+      done_ += mine;
+      if (done_ == nchunks_) done_cv_.notify_all();
+    }
+  }
+
+  std::vector<std::thread> th_;
+  std::mutex mu_;
+  std::condition_variable cv_, done_cv_;
+  const std::vector<Seg>* segs_ = nullptr;
+  size_t nchunks_ = 0, done_ = 0;
+  std::atomic<size_t> next_{0};
+  uint64_t job_ = 0;
+  bool stop_ = false;
+};
+
+// Copy threads of a cache: half the host's cores, at most 8, counting the caller.
+int copy_workers() {
+  const unsigned hc = std::thread::hardware_concurrency();
+  const int n = hc >= 2 ? (int)std::min(8u, hc / 2) : 1;
+  return n - 1;
+}
 
 }  // namespace
 
@@ -72,6 +182,7 @@ struct moe_w4a16_cache {
   std::vector<cudaEvent_t> stage_ev;  // transfer completion of each entry
   std::vector<bool> stage_live;
   int next_stage = 0;
+  CopyPool* pool = nullptr;           // host threads of the backing -> staging copies
   int32_t* tables_dev = nullptr;      // kTableRing x E
   int32_t* tables_host = nullptr;     // pinned kTableRing x E
   cudaEvent_t table_ev[kTableRing] = {};
@@ -173,15 +284,17 @@ moe_w4a16_status transport_one(moe_w4a16_cache* c, int expert, int row, cudaStre
   uint8_t* dp = c->dstage + (size_t)j * c->stage_entry;
   size_t off = 0;
   size_t qoff[3], soff[3];
+  std::vector<CopyPool::Seg> segs;
   for (int m = 0; m < 3; ++m) {
     qoff[m] = off;
-    std::memcpy(hp + off, c->bq[m] + (size_t)expert * c->qbytes[m], c->qbytes[m]);
+    segs.push_back({hp + off, c->bq[m] + (size_t)expert * c->qbytes[m], c->qbytes[m]});
     off += align256(c->qbytes[m]);
     soff[m] = off;
-    std::memcpy(hp + off, reinterpret_cast<const uint8_t*>(c->bs[m]) + (size_t)expert * c->sbytes[m],
-                c->sbytes[m]);
+    segs.push_back({hp + off, reinterpret_cast<const uint8_t*>(c->bs[m]) + (size_t)expert * c->sbytes[m],
+                    c->sbytes[m]});
     off += align256(c->sbytes[m]);
   }
+  c->pool->copy(segs);
   e = cudaMemcpyAsync(dp, hp, off, cudaMemcpyHostToDevice, st);
   const MatLayout* mats[3] = {&c->h->lay.gate, &c->h->lay.up, &c->h->lay.down};
   uint8_t* slot_base = c->h->pool + (size_t)row * c->h->lay.bytes;
@@ -285,6 +398,8 @@ void init_state(moe_w4a16_cache* c, const int32_t* initial, int32_t n_initial) {
 }
 
 void free_transport(moe_w4a16_cache* c) {
+  delete c->pool;
+  c->pool = nullptr;
   for (auto& kv : c->leases)
     if (kv.second.ev) cudaEventDestroy(kv.second.ev);
   c->leases.clear();
@@ -347,6 +462,7 @@ moe_w4a16_status moe_w4a16_cache_create(moe_w4a16_handle* h, const moe_w4a16_cac
   if (e == cudaSuccess) e = cudaMalloc(&c->tables_dev, (size_t)kTableRing * E * sizeof(int32_t));
   c->stage_ev.assign(ns, nullptr);
   c->stage_live.assign(ns, false);
+  c->pool = new CopyPool(copy_workers());
   for (int j = 0; j < ns && e == cudaSuccess; ++j) e = cudaEventCreateWithFlags(&c->stage_ev[j], cudaEventDisableTiming);
   for (int k = 0; k < kTableRing && e == cudaSuccess; ++k)
     e = cudaEventCreateWithFlags(&c->table_ev[k], cudaEventDisableTiming);
