@@ -62,9 +62,10 @@ CASES = [
     (3, 0, "fused"),
     (12, 0, "fused"),
     (3, F.FORCE_GEMV | F.UNFUSED, "cluster"),
-    (12, F.FORCE_GEMV | F.UNFUSED, "cooperative"),
+    (12, F.FORCE_GEMV | F.UNFUSED, "cooperative phases on one cluster"),
     (70, F.FORCE_GEMV, "cooperative"),
     (3, F.FORCE_GEMM, "cluster"),
+    (40, F.FORCE_GEMM, "cooperative phases on one cluster, x rows gathered"),
     (70, F.FORCE_GEMM, "cooperative"),
     (600, F.FORCE_GEMM, "cooperative, two CTAs per SM"),
 ]

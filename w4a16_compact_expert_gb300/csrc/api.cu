@@ -428,7 +428,7 @@ moe_w4a16_status moe_w4a16_forward(moe_w4a16_handle* h, const void* x, int32_t T
                      gemm_shapes_supported(h->cfg.hidden, h->cfg.inter));
   const bool fused_route = T <= ROUTE_FUSED_MAX_T;
   c.ksplit = 1;
-  c.tile_tokens = 256;   // token chunk of the grouped GEMM
+  c.tile_tokens = offload ? 256 : gemm_tile_tokens(T, c.k, c.E);   // token chunk of the grouped GEMM
   int ma = c.E;
   if ((long long)T * c.k < ma) ma = T * c.k;
   if (h->cfg.num_slots < ma) ma = h->cfg.num_slots;

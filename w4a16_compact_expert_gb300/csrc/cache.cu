@@ -68,7 +68,6 @@ class CopyPool {
     cv_.notify_all();
     for (auto& t : th_) t.join();
   }
-  int threads() const { return (int)th_.size() + 1; }
 
   // Copies every segment; returns when all bytes are in place.
   void copy(const std::vector<Seg>& segs) {

@@ -4,8 +4,9 @@
 // The compact int4 weights are the MMA A operand: two 128-row A matrices per
 // tile share every token stage (gate/up: the gate and up rows m0 .. m0 + 127;
 // down: rows m0 .. m0 + 255 of the down matrix as two halves).  The tokens of
-// one expert are the N dimension (a token chunk of <= 256, padded only to a
-// multiple of 16, so ragged expert loads waste little work).  Per 64-wide K
+// one expert are the N dimension (a token chunk of <= 256, or <= 128 in the
+// narrow variant, padded only to a multiple of 16, so ragged expert loads
+// waste little work).  Per 64-wide K
 // step:
 //   producer warp : 4-D TMA loads fetch the int4 chunks of the 8 row tiles of
 //                   each A matrix (and, at scale-block starts, their block
@@ -17,11 +18,14 @@
 //                   swizzled K-major A ring (the only place an expanded value
 //                   exists: one 64-wide K step of 2 x 128 rows, per CTA)
 //   MMA warp      : one thread issues tcgen05.mma M128 x N x K16 for each A
-//                   matrix into the two 256-column halves of one TMEM
-//                   accumulator and commits stage releases
+//                   matrix into the two halves of one TMEM accumulator (the
+//                   narrow variant alternates between two accumulators of
+//                   2 x 128 columns) and commits stage releases
 //   epilogue      : tcgen05.ld of the accumulator; gate/up: h = SiLU(g) * u
-//                   rounded to FP16; down: y [pair][H] FP16.  Split over the 4
-//                   epilogue warps and the 8 dequant warps, a third each
+//                   rounded to FP16; down: y [pair][H] FP16.  With one
+//                   accumulator split over the 4 epilogue warps and the 8
+//                   dequant warps, a third each; with two, the 4 epilogue
+//                   warps alone, under the next tile's MMAs
 // A last kernel gathers out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order.
 // Every wait is bounded (status word + early exit), nothing spins forever.
 // Sources: compact weights converted in-kernel with FP32 accumulation stages
@@ -35,38 +39,92 @@
 namespace {
 
 constexpr int kMTile = 128;     // weight rows per tile (MMA M)
-constexpr int kNMax = 256;      // tokens per tile (MMA N, max)
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of FP16)
-constexpr int kDqWarps = 8;     // warps 0-7 dequant (one 16-row tile each)
-constexpr int kThreads = 480;   // + warps 8-11 epilogue, 12 int4 producer, 13 token producer, 14 MMA
-constexpr int kWarpProd = 12, kWarpProdB = 13, kWarpMma = 14;   // warps 8-11: epilogue
+constexpr int kDqWarps = 8;     // dequant warps of one group (one 16-row tile of each A matrix each)
 constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;
 
-template <bool GU>
+// NMAX: tokens per tile (MMA N, max).
+//  256 (prefill): many tokens per weight byte.  The dequant warps write the
+//      FP16 weights into a shared-memory A ring; a shallow int4 ring keeps the
+//      tensor cores fed; one accumulator of 2 x 256 TMEM columns.
+//  32 (a few to ~16 tokens per expert): few tokens per weight byte, so the
+//      tile must stream its weights at HBM speed.  There every 64-wide K step
+//      of the shared-memory design cost ~1,400 cycles whatever the ring
+//      depths: the MMA thread spent ~550 cycles issuing its 8 MMAs (M = 128,
+//      N <= 64 costs ~60 cycles per MMA whatever N) and ~800 on the fixed
+//      cost of a step (barrier wait, commits, loop).  So here a pipeline
+//      stage is two 64-wide K chunks (16 MMAs per barrier round trip), the
+//      dequant warps store the FP16 weights straight into tensor memory
+//      (tcgen05.st, one row per TMEM lane, no shared-memory A ring) and the
+//      MMA takes A from there; two groups of dequant warps take alternate
+//      stages, a deep int4 ring covers HBM latency, and two accumulators let
+//      one tile's epilogue run under the next tile's MMAs.
+template <bool GU, int NMAX>
 struct Cfg {
+  static constexpr bool kWide = NMAX > 64;
+  static constexpr bool kTS = !kWide;                 // A (weights) from tensor memory
+  static constexpr int kCh = kTS ? 2 : 1;             // 64-wide K chunks per A / int4 stage
   // two 128-row A tiles share every token stage: gate and up (gate/up), rows
   // m0 and m0 + 128 of the down matrix (down)
   static constexpr int kMats = 2;
-  static constexpr int kStagesA = 3;             // dequantised FP16 A stages
-  static constexpr int kStagesB = 3;
-  static constexpr int kStagesRaw = 3;             // int4 chunks (+ scales) from HBM
+  static constexpr int kAcc = kWide ? 1 : 2;          // accumulators
+  static constexpr int kHalf = kWide ? 256 : NMAX;    // TMEM column of the second A matrix's half
+  // Warp roles: kDqGroups groups of 8 dequant warps (group g converts the
+  // K steps s with s % kDqGroups == g), then 4 epilogue warps (TMEM lane
+  // quarters 0-3), the int4 producer, the token producer and the MMA warp.
+  static constexpr int kDqGroups = kWide ? 1 : 2;
+  static constexpr int kDqAll = kDqWarps * kDqGroups;
+  static constexpr int kWarpProd = kDqAll + 4, kWarpProdB = kDqAll + 5, kWarpMma = kDqAll + 6;
+  static constexpr int kThreads = (kDqAll + 7) * 32;
+  // every int4 stage carries its block scales when a group does not see the
+  // first K step of every block
+  static constexpr bool kScalesEveryStage = kDqGroups > 1;
+  static constexpr int kStagesA = 3;                  // dequantised FP16 A stages
+  static constexpr int kASmemStages = kTS ? 0 : kStagesA;
+  static constexpr int kTmemA = 2 * kAcc * kHalf;     // TS: first TMEM column of the A stages
+  static constexpr int kTmemAMat = kCh * kBK / 2;     // TS: columns of one matrix in an A stage (FP16 pairs)
+  static constexpr int kTmemAStage = kMats * kTmemAMat;
+  static constexpr int kStagesB = kTS ? 8 : 3;
+  static constexpr int kBoxRows = kWide ? 64 : 16;    // token rows per TMA box of a B stage
   static constexpr int kAMat = kMTile * kBK * 2;          // 16 KB per matrix per stage
   static constexpr int kABytes = kMats * kAMat;
-  static constexpr int kBBytes = kNMax * kBK * 2;         // 32 KB
-  // int4 chunks of 8 row tiles per matrix, then (at block boundaries) the
-  // 16 block scales of the same 8 row tiles per matrix
+  static constexpr int kBBytes = NMAX * kBK * 2;          // 32 KB (256) or 4 KB (32)
+  // per K chunk, the int4 chunks of 8 row tiles per matrix; then (at block
+  // boundaries, or in every stage) the 16 block scales of the same 8 row
+  // tiles per matrix
   static constexpr int kRawQ = kMats * 8 * 512;
-  static constexpr int kRawBytes = kRawQ + kMats * 8 * 32;
+  static constexpr int kRawBytes = kCh * kRawQ + kMats * 8 * 32;
+  static constexpr int kSchedBytes = (4 * (kMaxE + 1) + 4) * 4;
+  // int4 chunks (+ scales) from HBM: whatever the other rings leave
+  static constexpr int kFixed = kASmemStages * kABytes + kStagesB * kBBytes + kSchedBytes +
+                                (2 * kStagesA + 2 * kStagesB + 4) * 8 + 16 + 1024;
+  static constexpr int kRawFit = (227 * 1024 - kFixed) / (kRawBytes + 16);
+  static constexpr int kStagesRaw = kWide ? 3 : (kRawFit < 16 ? kRawFit : 16);
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kStagesA * kABytes;
+  static constexpr int kOffB = kOffA + kASmemStages * kABytes;
   static constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
   static constexpr int kOffSched = kOffRaw + kStagesRaw * kRawBytes;   // 4 x (kMaxE + 1) ints + count
-  static constexpr int kOffBar = kOffSched + (4 * (kMaxE + 1) + 4) * 4;
+  static constexpr int kOffBar = kOffSched + kSchedBytes;
   static constexpr int kNumBars = 2 * kStagesRaw + 2 * kStagesA + 2 * kStagesB + 4;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;   // + TMEM slot + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kStagesRaw >= 3, "int4 ring depth");
+  static_assert(kRawBytes % 128 == 0 && kBBytes % 1024 == 0, "ring alignment");
+  static_assert(!kTS || kTmemA + kStagesA * kTmemAStage <= (int)kTmemCols, "tensor memory budget");
 };
+
+// K steps per token stage for a tile of n tokens: a stage holds NMAX rows of
+// one K step, or, for fewer tokens, that many bytes of several consecutive K
+// steps (each a K-major swizzled block of the tile's rows rounded up to the
+// TMA box), so that a small tile keeps as many K steps in flight as the
+// bytes allow.
+template <class C>
+DEV_INLINE int kb_per_stage(int n) {
+  const int rows = (n + C::kBoxRows - 1) / C::kBoxRows * C::kBoxRows;
+  const int kpb = C::kBBytes / (rows * 128);
+  return kpb > 0 ? kpb : 1;
+}
 
 struct Ring {
   int i = 0;
@@ -124,7 +182,8 @@ DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
 }
 
 // Tile t -> (active expert, token chunk, weight-row tile).  Chunks split an
-// expert's rows into ceil(count / 256) near-equal parts.
+// expert's rows into ceil(count / tile_tokens) near-equal parts (the routing
+// kernels wrote that prefix into act_tile).
 DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, int mstep, Tile& out) {
   if (s.n <= 0) return false;
   if (t >= s.hi) return false;
@@ -165,12 +224,12 @@ DEV_INLINE void st_shared_v4_b32(uint32_t addr, uint32_t v0, uint32_t v1, uint32
 // execution slots of the active experts [c.ub0, c.ub1) (tmA0 / tmA1: 3-D maps,
 // 128 rows x 64 K per load, 128-byte swizzled straight into the A ring), no
 // dequantisation; the tile schedule covers only those experts.
-template <bool GU, bool DENSE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GU, bool DENSE, int NMAX>
+__global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
     grouped_gemm_kernel(FwdCtx c, const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmS0,
                         const __grid_constant__ CUtensorMap tmS1) {
-  using C = Cfg<GU>;
+  using C = Cfg<GU, NMAX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -202,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 12);   // one arrive per warp that reads the accumulator
+      mbar_init(&acc_empty[s], C::kAcc == 1 ? 12 : 4);   // one arrive per warp that reads the accumulator
     }
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == C::kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -219,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // gate/up: tiles of 128 rows of gate and up; down: tiles of 256 rows, the
   // second 128 rows as the second A matrix (row offset m1off)
   const int mstep = GU ? kMTile : 2 * kMTile, m1off = GU ? 0 : kMTile;
-  const int K = (int)LA.k, nks = K / kBK, mtiles = (int)LA.rows / mstep;
+  // nks: 64-wide K chunks of a tile (token stages); nst: A / int4 stages
+  const int K = (int)LA.k, nks = K / kBK, nst = nks / C::kCh, mtiles = (int)LA.rows / mstep;
   if (DENSE) {
     sch.lo = sch.tile[min(c.ub0, sch.n)] * mtiles;
     sch.hi = sch.tile[min(c.ub1, sch.n)] * mtiles;
@@ -227,16 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     sch.lo = 0;
     sch.hi = sch.n > 0 ? sch.tile[sch.n] * mtiles : 0;
   }
-  const int nacc = 1;   // one accumulator: the two A matrices' halves fill the 512 columns
+  const int nacc = C::kAcc;
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
-  // chunks [ch0, ch1): gate/up -> h = SiLU(g) * u (FP16), down -> y (FP16) of
-  // rows m0 + row (first accumulator half) and m0 + 128 + row (second).  The
-  // single accumulator puts the epilogue on the MMA's critical path: it is
-  // split over the 4 epilogue warps and the 8 dequant warps (which wait for the
-  // MMA at that point anyway), a third each.
-  auto epilogue_chunks = [&](const Tile& et, int ch0, int ch1) {
+  // chunks [ch0, ch1) of accumulator `ai`: gate/up -> h = SiLU(g) * u (FP16),
+  // down -> y (FP16) of rows m0 + row (first accumulator half) and m0 + 128 +
+  // row (second).  A single accumulator puts the epilogue on the MMA's
+  // critical path: it is then split over the 4 epilogue warps and the 8
+  // dequant warps (which wait for the MMA at that point anyway), a third each.
+  auto epilogue_chunks = [&](const Tile& et, int ch0, int ch1, int ai) {
     const int qw = warp & 3, row = qw * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(qw * 32) << 16);
+    const uint32_t taddr = tmem + (uint32_t)(ai * 2 * C::kHalf) + ((uint32_t)(qw * 32) << 16);
     for (int col0 = ch0 * 32; col0 < ch1 * 32 && col0 < et.n; col0 += 32) {
       // the 32 columns' pair indices (down) or PRENORM row scales (gate/up):
       // one coalesced load per chunk, broadcast below
@@ -246,36 +306,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!GU) my_pair = c.sorted[et.r0 + col0 + lane];
         else if (c.flags & 2u) my_rn = c.rnorm[c.sorted[et.r0 + col0 + lane] / c.k];
       }
-      uint32_t va[32], vb[32];
-      tmem_ld32(taddr + col0, va);
-      tmem_ld32(taddr + 256u + col0, vb);
-      tmem_wait_ld();
+      // 32 columns per TMEM load, or 2 x 16 in the narrow variant (whose 23
+      // warps leave fewer registers per thread)
+      constexpr int W = C::kWide ? 32 : 16;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int nn = col0 + j;
-        const int pair = GU ? 0 : __shfl_sync(0xffffffffu, my_pair, j);
-        if (nn < et.n) {
-          if (GU) {
-            float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
-            if (c.flags & 2u) {
-              const float r = __shfl_sync(0xffffffffu, my_rn, j);
-              gv *= r;
-              uv *= r;
+      for (int sub = 0; sub < 32; sub += W) {
+        if (col0 + sub >= et.n) break;
+        uint32_t va[W], vb[W];
+        tmem_ld_cols(taddr + (uint32_t)(col0 + sub), va);
+        tmem_ld_cols(taddr + (uint32_t)(C::kHalf + col0 + sub), vb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          const int nn = col0 + sub + j;
+          const int pair = GU ? 0 : __shfl_sync(0xffffffffu, my_pair, sub + j);
+          if (nn < et.n) {
+            if (GU) {
+              float gv = __uint_as_float(va[j]), uv = __uint_as_float(vb[j]);
+              if (c.flags & 2u) {
+                const float r = __shfl_sync(0xffffffffu, my_rn, sub + j);
+                gv *= r;
+                uv *= r;
+              }
+              c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
+            } else {
+              // the expert's output rounded once to FP16 (an activation), the
+              // combine then sums the k ranks in FP32
+              __half* yr = reinterpret_cast<__half*>(c.ybuf) + (size_t)pair * c.H + et.m0 + row;
+              yr[0] = __float2half_rn(__uint_as_float(va[j]));
+              yr[kMTile] = __float2half_rn(__uint_as_float(vb[j]));
             }
-            c.hbuf[(size_t)(et.r0 + nn) * c.I + et.m0 + row] = __float2half_rn(silu_mul(gv, uv));
-          } else {
-            // the expert's output rounded once to FP16 (an activation), the
-            // combine then sums the k ranks in FP32
-            __half* yr = reinterpret_cast<__half*>(c.ybuf) + (size_t)pair * c.H + et.m0 + row;
-            yr[0] = __float2half_rn(__uint_as_float(va[j]));
-            yr[kMTile] = __float2half_rn(__uint_as_float(vb[j]));
           }
         }
       }
     }
   };
 
-  if (DENSE && warp == kWarpProd) {
+  if (DENSE && warp == C::kWarpProd) {
     // ----------------------------------------- FP16 A producer (comparison)
     if (lane == 0) {
       Ring ra;
@@ -298,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpProd) {
+  } else if (warp == C::kWarpProd) {
     // ------------------------------------------------- int4 chunk producer
     if (lane == 0) {
       Ring rr;
@@ -306,19 +373,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         Tile tl;
         if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         bool ok = true;
-        for (int ks = 0; ks < nks; ++ks) {
+        for (int ks = 0; ks < nst; ++ks) {
           if (!mbar_wait_bounded(&raw_empty[rr.i], rr.ph ^ 1u, c.status)) {
             ok = false;
             break;
           }
           uint8_t* dst = smem + C::kOffRaw + rr.i * C::kRawBytes;
-          const bool blk = (ks & 3) == 0;   // first K step of a scale block: its scales come along
-          mbar_expect_tx(&raw_full[rr.i], blk ? (uint32_t)C::kRawBytes : (uint32_t)C::kRawQ);
-          tma_load_4d(dst, &tmA0, 0, ks, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
-          tma_load_4d(dst + 8 * 512, &tmA1, 0, ks, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
+          const int kc0 = ks * C::kCh;   // first K chunk of the stage
+          // first K chunk of a scale block (or every stage): its scales come along
+          const bool blk = C::kScalesEveryStage || (kc0 & 3) == 0;
+          mbar_expect_tx(&raw_full[rr.i], blk ? (uint32_t)C::kRawBytes : (uint32_t)(C::kCh * C::kRawQ));
+#pragma unroll
+          for (int h = 0; h < C::kCh; ++h) {
+            tma_load_4d(dst + h * C::kRawQ, &tmA0, 0, kc0 + h, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+            tma_load_4d(dst + h * C::kRawQ + 8 * 512, &tmA1, 0, kc0 + h, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
+          }
           if (blk) {
-            tma_load_4d(dst + C::kRawQ, &tmS0, 0, ks >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
-            tma_load_4d(dst + C::kRawQ + 256, &tmS1, 0, ks >> 2, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
+            uint8_t* sdst = dst + C::kCh * C::kRawQ;
+            tma_load_4d(sdst, &tmS0, 0, kc0 >> 2, tl.m0 / 16, tl.slot, &raw_full[rr.i]);
+            tma_load_4d(sdst + 256, &tmS1, 0, kc0 >> 2, (tl.m0 + m1off) / 16, tl.slot, &raw_full[rr.i]);
           }
           rr.next(C::kStagesRaw);
         }
@@ -326,30 +399,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpProdB) {
+  } else if (warp == C::kWarpProdB) {
     // ------------------------------------------------- token tile producer
     if (lane == 0) {
       Ring rb;
       for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
         Tile tl;
         if (!get_tile(sch, t, mtiles, mstep, tl)) break;
-        const int nq = (tl.n + 63) / 64;
+        constexpr int kBox = C::kBoxRows;
+        const int nq = (tl.n + kBox - 1) / kBox;
+        const int kpb = kb_per_stage<C>(tl.n);
         bool ok = true;
-        for (int ks = 0; ks < nks; ++ks) {
+        for (int ks0 = 0; ks0 < nks; ks0 += kpb) {
           if (!mbar_wait_bounded(&b_empty[rb.i], rb.ph ^ 1u, c.status)) {
             ok = false;
             break;
           }
+          const int nk = min(kpb, nks - ks0);
           uint8_t* bdst = smem + C::kOffB + rb.i * C::kBBytes;
-          mbar_expect_tx(&b_full[rb.i], (uint32_t)nq * 64u * 128u);
-          for (int q = 0; q < nq; ++q) tma_load_2d(bdst + q * 8192, &tmB, ks * kBK, tl.r0 + q * 64, &b_full[rb.i]);
+          mbar_expect_tx(&b_full[rb.i], (uint32_t)(nk * nq * kBox * 128));
+          for (int j = 0; j < nk; ++j)
+            for (int q = 0; q < nq; ++q)
+              tma_load_2d(bdst + (j * nq + q) * kBox * 128, &tmB, (ks0 + j) * kBK, tl.r0 + q * kBox, &b_full[rb.i]);
           rb.next(C::kStagesB);
         }
         if (!ok) break;
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == C::kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       Ring ra, rb, racc;
@@ -359,29 +437,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!get_tile(sch, t, mtiles, mstep, tl)) break;
         const int n16 = (tl.n + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kMTile, n16);
+        const int kpb = kb_per_stage<C>(tl.n);
+        const uint32_t bsub = (uint32_t)(((tl.n + C::kBoxRows - 1) / C::kBoxRows) * C::kBoxRows * 128);
         if (!mbar_wait_bounded(&acc_empty[racc.i], racc.ph ^ 1u, c.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem;
-        for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait_bounded(&a_full[ra.i], ra.ph, c.status) ||
-              !mbar_wait_bounded(&b_full[rb.i], rb.ph, c.status)) {
+        const uint32_t d0 = tmem + (uint32_t)(racc.i * 2 * C::kHalf);
+        int kc = 0, j = 0;   // K chunk of the tile; K chunk inside the token stage
+        for (int ks = 0; ks < nst && ok; ++ks) {
+          if (!mbar_wait_bounded(&a_full[ra.i], ra.ph, c.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + C::kOffA + ra.i * C::kABytes);
-          const uint32_t b_base = smem_u32(smem + C::kOffB + rb.i * C::kBBytes);
 #pragma unroll
-          for (int k16 = 0; k16 < kBK / 16; ++k16) {
-            const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
-            const uint32_t acc = (ks | k16) != 0;
-            umma_f16_ss(d0, sw128_desc(a_base + k16 * 32), bdesc, idesc, acc);
-            umma_f16_ss(tmem + 256u, sw128_desc(a_base + C::kAMat + k16 * 32), bdesc, idesc, acc);
+          for (int h = 0; h < C::kCh; ++h, ++kc) {
+            if (j == 0) {
+              if (!mbar_wait_bounded(&b_full[rb.i], rb.ph, c.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t b_base = smem_u32(smem + C::kOffB + rb.i * C::kBBytes) + (uint32_t)j * bsub;
+            if constexpr (C::kTS) {
+              const uint32_t a_t = tmem + (uint32_t)(C::kTmemA + ra.i * C::kTmemAStage + h * (kBK / 2));
+#pragma unroll
+              for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
+                const uint32_t acc = (kc | k16) != 0;
+                umma_f16_ts(d0, a_t + (uint32_t)(k16 * 8), bdesc, idesc, acc);
+                umma_f16_ts(d0 + (uint32_t)C::kHalf, a_t + (uint32_t)(C::kTmemAMat + k16 * 8), bdesc, idesc, acc);
+              }
+            } else {
+              const uint32_t a_base = smem_u32(smem + C::kOffA + ra.i * C::kABytes);
+#pragma unroll
+              for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
+                const uint32_t acc = (kc | k16) != 0;
+                umma_f16_ss(d0, sw128_desc(a_base + k16 * 32), bdesc, idesc, acc);
+                umma_f16_ss(d0 + (uint32_t)C::kHalf, sw128_desc(a_base + C::kAMat + k16 * 32), bdesc, idesc, acc);
+              }
+            }
+            if (++j == kpb || kc == nks - 1) {   // the token stage's last K chunk
+              umma_commit(&b_empty[rb.i]);
+              rb.next(C::kStagesB);
+              j = 0;
+            }
           }
+          if (!ok) break;
           umma_commit(&a_empty[ra.i]);
-          umma_commit(&b_empty[rb.i]);
           ra.next(C::kStagesA);
-          rb.next(C::kStagesB);
         }
         if (!ok) break;
         umma_commit(&acc_full[racc.i]);
@@ -389,9 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < kDqWarps) {
+  } else if (warp < C::kDqAll) {
     // ------------------------------------------------------------ dequant
     const int g = lane >> 2, cq = lane & 3;
+    const int dw = warp % kDqWarps, grp = warp / kDqWarps;   // 16-row tile, group
+    int seq = 0;                                             // K steps of this CTA so far
     Ring rr, ra, racc;
     bool ok = true;
     Tile pend = {0, 0, 0, 0};   // gate/up: the tile whose epilogue share is still due
@@ -402,11 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) return false;
       tc_fence_after();
       const int nch = (pend.n + 31) / 32, part = 1 + (warp >> 2);
-      epilogue_chunks(pend, part * nch / 3, (part + 1) * nch / 3);
+      epilogue_chunks(pend, part * nch / 3, (part + 1) * nch / 3, racc.i);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
-      racc.next(1);
+      racc.next(nacc);
       have = false;
       return true;
     };
@@ -415,16 +522,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!get_tile(sch, t, mtiles, mstep, pend) || !epilogue_share()) break;
       }
     }
-    for (int t = sch.lo + blockIdx.x; ok && !DENSE; t += gridDim.x) {
+    if constexpr (C::kTS) {
+      // One row of one A matrix per thread, straight into tensor memory: warp
+      // dw converts matrix dw / 4, rows 32 (warp % 4) + lane (its TMEM lane
+      // quarter).  Row m of the 128-row matrix is row r = m % 16 of 16-row tile
+      // m / 16; in a 512-byte int4 chunk its words sit in the 64 bytes of lane
+      // group r % 8 (lanes 4 (r % 8) + c, c = 0..3), word j of lane c holding
+      // K = 16c + 4j + {0, 1} in its bits 0-3 / 16-19 and K + {2, 3} in bits
+      // 8-11 / 24-27 (rows 8-15 of the tile: the nibbles 4 bits higher).  The
+      // FP16 pair of K = 2p, 2p + 1 goes to TMEM column p of the stage.
+      const int mat = dw >> 2, qd = warp & 3;
+      const int m = qd * 32 + lane, rt = m >> 4, r = m & 15;
+      const uint32_t nshift = (uint32_t)(r >> 3) * 4u;
+      const uint32_t trow = tmem + (uint32_t)(C::kTmemA + mat * C::kTmemAMat) + ((uint32_t)(qd * 32) << 16);
+      for (int t = sch.lo + blockIdx.x; ok; t += gridDim.x) {
+        Tile tl;
+        if (!get_tile(sch, t, mtiles, mstep, tl)) break;
+        for (int ks = 0; ks < nst; ++ks) {
+          if ((seq++ % C::kDqGroups) != grp) {   // the other group's K step
+            rr.next(C::kStagesRaw);
+            ra.next(C::kStagesA);
+            continue;
+          }
+          if (!mbar_wait_bounded(&raw_full[rr.i], rr.ph, c.status)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* raw = smem + C::kOffRaw + rr.i * C::kRawBytes;
+          const __half2 sc =
+              __half2half2(reinterpret_cast<const __half*>(raw + C::kCh * C::kRawQ + mat * 256 + rt * 32)[r]);
+          if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < C::kCh; ++h) {
+            const uint8_t* qp = raw + h * C::kRawQ + (mat * 8 + rt) * 512 + (r & 7) * 64;
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(qp + 16 * i);
+            uint32_t o[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t w = wv[j] >> nshift;
+                o[8 * i + 2 * j] = dequant_pair(w, sc);
+                o[8 * i + 2 * j + 1] = dequant_pair(w >> 8, sc);
+              }
+            }
+            tmem_st32(trow + (uint32_t)(ra.i * C::kTmemAStage + h * (kBK / 2)), o);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          // the int4 slot is released after its words were used (see below)
+          if (lane == 0) {
+            mbar_arrive(&a_full[ra.i]);
+            mbar_arrive(&raw_empty[rr.i]);
+          }
+          rr.next(C::kStagesRaw);
+          ra.next(C::kStagesA);
+        }
+      }
+    }
+    for (int t = sch.lo + blockIdx.x; ok && !DENSE && !C::kTS; t += gridDim.x) {
       Tile tl;
       if (!get_tile(sch, t, mtiles, mstep, tl)) break;
       // the scales of the thread's rows for the current block (read from the
-      // raw stage that starts the block)
+      // raw stage that starts the block, or from every stage)
       __half2 slo[2][1], shi[2][1];
-      for (int ks = 0; ks < nks; ++ks) {
+      for (int ks = 0; ks < nst; ++ks) {
+        if (C::kDqGroups > 1 && (seq++ % C::kDqGroups) != grp) {   // the other group's K step
+          rr.next(C::kStagesRaw);
+          ra.next(C::kStagesA);
+          continue;
+        }
         // the A ring is full at this point: the MMA waits for the previous
         // tile's epilogue before it takes stage 0 of this one
-        if (have && ks == C::kStagesA && !epilogue_share()) {
+        if (C::kAcc == 1 && have && ks == C::kStagesA && !epilogue_share()) {
           ok = false;
           break;
         }
@@ -434,16 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint4 q[2][1];
         const uint8_t* raw = smem + C::kOffRaw + rr.i * C::kRawBytes;
-        if ((ks & 3) == 0) {
+        if (C::kScalesEveryStage || (ks & 3) == 0) {
 #pragma unroll
           for (int m = 0; m < C::kMats; ++m) {
-            const __half* sc = reinterpret_cast<const __half*>(raw + C::kRawQ + m * 256 + warp * 32);
+            const __half* sc = reinterpret_cast<const __half*>(raw + C::kRawQ + m * 256 + dw * 32);
             slo[m][0] = __half2half2(sc[g]);
             shi[m][0] = __half2half2(sc[g + 8]);
           }
         }
 #pragma unroll
-        for (int m = 0; m < C::kMats; ++m) q[m][0] = *reinterpret_cast<const uint4*>(raw + (m * 8 + warp) * 512 + lane * 16);
+        for (int m = 0; m < C::kMats; ++m) q[m][0] = *reinterpret_cast<const uint4*>(raw + (m * 8 + dw) * 512 + lane * 16);
         if (!mbar_wait_bounded(&a_empty[ra.i], ra.ph ^ 1u, c.status)) {
           ok = false;
           break;
@@ -453,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 0; m < C::kMats; ++m) {
 #pragma unroll
           for (int tt = 0; tt < 1; ++tt) {
-            const int row = warp * 16 + g;   // and row + 8 (same swizzle phase)
+            const int row = dw * 16 + g;   // and row + 8 (same swizzle phase)
             const uint32_t rlo = abase + m * C::kAMat + row * 128;
             const uint32_t rhi = rlo + 8 * 128;
             const uint32_t sw = (uint32_t)(row & 7);
@@ -487,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rr.next(C::kStagesRaw);
         ra.next(C::kStagesA);
       }
-      if (ok) {
+      if (ok && C::kAcc == 1) {
         pend = tl;
         have = true;
       }
@@ -503,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) break;
       tc_fence_after();
       const int nch = (tl.n + 31) / 32;
-      epilogue_chunks(tl, 0, nch / 3);
+      epilogue_chunks(tl, 0, C::kAcc == 1 ? nch / 3 : nch, racc.i);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[racc.i]);
@@ -513,24 +691,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == C::kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // out[t] = (x[t]) + sum_j w[t,j] y[t*k+j] in rank order j, FP32, then FP16.
-// A CTA covers 2048 hidden values of one token (8 per thread, 16-byte loads
-// of the FP16 y rows); the token's weights (0 for an absent expert) are read
-// once into shared memory so that the y loads of all ranks are independent.
-__global__ void __launch_bounds__(256) combine_kernel(FwdCtx c) {
+// A CTA covers 512 hidden values of one token (8 per thread, 16-byte loads
+// of the FP16 y rows: small CTAs, so that a few tokens still spread over
+// the SMs); the token's weights (0 for an absent expert) are read once into
+// shared memory so that the y loads of all ranks are independent.
+constexpr int kCombineThreads = 64;
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(FwdCtx c) {
   __shared__ float ws[32];
   pdl_wait();
   pdl_trigger();
   const int H = c.H, k = c.k;
-  const int blocks_per_tok = (H / 8 + 255) / 256;
+  const int blocks_per_tok = (H / 8 + kCombineThreads - 1) / kCombineThreads;
   const int t = blockIdx.x / blocks_per_tok;
-  const int v = (blockIdx.x % blocks_per_tok) * 256 + threadIdx.x;   // 8-value vector inside the row
+  const int v = (blockIdx.x % blocks_per_tok) * kCombineThreads + threadIdx.x;   // 8-value vector inside the row
   if (threadIdx.x < k) {
     const int p = t * k + threadIdx.x;
     ws[threadIdx.x] = c.table[c.ids[p]] >= 0 ? c.topw[p] : 0.f;
@@ -679,30 +859,45 @@ PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slot
   return pm;
 }
 
+int gemm_tile_tokens(int T, int k, int E) { return (long long)T * k <= 16ll * E ? 32 : 256; }
+
+// gate/up and down grouped GEMMs of one token-tile variant (c.tile_tokens
+// must equal NMAX: the routing kernels chunked the experts' rows with it)
+template <int NMAX>
+cudaError_t launch_gemm_pair(const FwdCtx& c, const PoolMaps& pm, cudaStream_t st, const StageEvents& se) {
+  using CG = Cfg<true, NMAX>;
+  using CD = Cfg<false, NMAX>;
+  const uint64_t P = (uint64_t)c.T * c.k;
+  CUtensorMap mx, mh;
+  if (!make_map(&mx, c.xp, P, (uint64_t)c.H, CG::kBoxRows) || !make_map(&mh, c.hbuf, P, (uint64_t)c.I, CD::kBoxRows))
+    return cudaErrorNotSupported;
+  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, false, NMAX>, CG::kSmem);
+  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, false, NMAX>, CD::kSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = c.num_sms > 0 ? c.num_sms : 148;
+  e = launch_pdl(grouped_gemm_kernel<true, false, NMAX>, dim3(grid), dim3(CG::kThreads), CG::kSmem, st, 1, c, mx, pm.q[0],
+                 pm.q[1], pm.sc[0], pm.sc[1]);
+  if (e == cudaSuccess) e = record_stage(se, 2, st);
+  if (e == cudaSuccess)
+    e = launch_pdl(grouped_gemm_kernel<false, false, NMAX>, dim3(grid), dim3(CD::kThreads), CD::kSmem, st, 1, c, mh,
+                   pm.q[2], pm.q[2], pm.sc[2], pm.sc[2]);
+  return e;
+}
+
 cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, bool gathered, cudaStream_t st,
                                 const StageEvents& se) {
   if (!gemm_shapes_supported(c.H, c.I) || !pm.ok) return cudaErrorNotSupported;
+  if (c.tile_tokens != 32 && c.tile_tokens != 256) return cudaErrorInvalidValue;
   const uint64_t P = (uint64_t)c.T * c.k;
-  CUtensorMap mx, mh;
-  if (!make_map(&mx, c.xp, P, (uint64_t)c.H, 64) || !make_map(&mh, c.hbuf, P, (uint64_t)c.I, 64))
-    return cudaErrorNotSupported;
-  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, false>, Cfg<true>::kSmem);
-  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, false>, Cfg<false>::kSmem);
-  if (e != cudaSuccess) return e;
-  const int grid = c.num_sms > 0 ? c.num_sms : 148;
+  cudaError_t e = cudaSuccess;
   if (!gathered)
     e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 1, st);
-  if (e == cudaSuccess)
-    e = launch_pdl(grouped_gemm_kernel<true, false>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx, pm.q[0],
-                   pm.q[1], pm.sc[0], pm.sc[1]);
-  if (e == cudaSuccess) e = record_stage(se, 2, st);
-  if (e == cudaSuccess)
-    e = launch_pdl(grouped_gemm_kernel<false, false>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh, pm.q[2],
-                   pm.q[2], pm.sc[2], pm.sc[2]);
+  if (e == cudaSuccess) e = c.tile_tokens == 32 ? launch_gemm_pair<32>(c, pm, st, se) : launch_gemm_pair<256>(c, pm, st, se);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 8 + 255) / 256))), dim3(256), 0, st, 1, c);
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 8 + kCombineThreads - 1) / kCombineThreads))),
+                   dim3(kCombineThreads), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }
@@ -743,8 +938,11 @@ cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, bool g
   CUtensorMap mx, mh;
   if (!make_map(&mx, c0.xp, P, (uint64_t)c0.H, 64) || !make_map(&mh, c0.hbuf, P, (uint64_t)c0.I, 64))
     return cudaErrorNotSupported;
-  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, true>, Cfg<true>::kSmem);
-  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, true>, Cfg<false>::kSmem);
+  using CG = Cfg<true, 256>;
+  using CD = Cfg<false, 256>;
+  if (c0.tile_tokens != 256) return cudaErrorInvalidValue;
+  cudaError_t e = opt_in_smem((const void*)grouped_gemm_kernel<true, true, 256>, CG::kSmem);
+  if (e == cudaSuccess) e = opt_in_smem((const void*)grouped_gemm_kernel<false, true, 256>, CD::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = c0.num_sms > 0 ? c0.num_sms : 148;
   if (!gathered)
@@ -757,16 +955,17 @@ cudaError_t launch_offload_experts(const FwdCtx& c0, const DenseMaps& dm, bool g
     c.ub1 = c.ub0 + c0.xslots < c0.max_active ? c.ub0 + c0.xslots : c0.max_active;
     e = launch_expand(c, st);
     if (e == cudaSuccess)
-      e = launch_pdl(grouped_gemm_kernel<true, true>, dim3(grid), dim3(kThreads), Cfg<true>::kSmem, st, 1, c, mx,
+      e = launch_pdl(grouped_gemm_kernel<true, true, 256>, dim3(grid), dim3(CG::kThreads), CG::kSmem, st, 1, c, mx,
                      dm.a[0], dm.a[1], dm.a[0], dm.a[1]);
     if (e == cudaSuccess)
-      e = launch_pdl(grouped_gemm_kernel<false, true>, dim3(grid), dim3(kThreads), Cfg<false>::kSmem, st, 1, c, mh,
+      e = launch_pdl(grouped_gemm_kernel<false, true, 256>, dim3(grid), dim3(CD::kThreads), CD::kSmem, st, 1, c, mh,
                      dm.a[2], dm.a[2], dm.a[2], dm.a[2]);
   }
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel, dim3((unsigned)(c0.T * ((c0.H / 8 + 255) / 256))), dim3(256), 0, st, 1, c0);
+    e = launch_pdl(combine_kernel, dim3((unsigned)(c0.T * ((c0.H / 8 + kCombineThreads - 1) / kCombineThreads))),
+                   dim3(kCombineThreads), 0, st, 1, c0);
   if (e == cudaSuccess) e = record_stage(se, 4, st);
   return e;
 }

@@ -102,6 +102,10 @@ cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEve
 
 // gemm_tc.cu: prefill regime (gather, gate/up GEMM, down GEMM, combine)
 bool gemm_shapes_supported(int H, int I);
+// Token tile of the grouped GEMM for T tokens (routing chunks each expert's
+// rows with it): 128 while the average expert sees at most 64 pairs (the
+// narrow variant: deep int4 ring, two accumulators), else 256.
+int gemm_tile_tokens(int T, int k, int E);
 
 // TMA maps over the whole slot pool for the grouped GEMM, built once per
 // handle: q, the packed int4 chunks of gate, up and down ([slot][row tile][K

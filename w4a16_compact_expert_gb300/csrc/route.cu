@@ -15,9 +15,10 @@
 //              permutation entirely in shared memory.
 //   larger T : one cooperative kernel (logits on the tensor cores, top-k,
 //              scan, scatter and, for the grouped GEMM, the x rows in sorted
-//              order: the forward's router), or four launches (logits, top-k,
-//              scan, scatter: the allocation-free router, which has no
-//              barrier counter of its own).
+//              order: the forward's router; up to 64 tokens the same phases
+//              on one 8-CTA thread-block cluster), or four launches (logits,
+//              top-k, scan, scatter: the allocation-free router, which has
+//              no barrier counter of its own).
 #include "route_dev.cuh"
 
 namespace {
@@ -438,6 +439,15 @@ DEV_INLINE bool coop_grid_barrier(unsigned long long* ctr, unsigned nblocks, Dev
 // they fit (counter 1).
 constexpr int kDirectBlocks = 64;
 
+// CL: the same phases on one thread-block cluster of kRouteClusterCTAs CTAs
+// (launched with programmatic dependent launch), the phase barriers being the
+// hardware cluster barrier (release / acquire at cluster scope, which orders
+// the global writes of one phase before the reads of the next): no grid-wide
+// counter round trips, for the few token blocks of 16 < T <= 64.
+constexpr int kRouteClusterCTAs = 8;
+constexpr int kRouteClusterMaxT = 64;
+
+template <bool CL>
 __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
   extern __shared__ __align__(16) uint8_t csm[];   // one logits tile (phase 0)
   __shared__ float lg[8][256];
@@ -453,6 +463,24 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
   const bool direct = nb <= kDirectBlocks;
   unsigned long long* bar = c.route_bar + (direct ? 0 : 1);   // one grid size per counter
   if (tid == 0) s_ok = 1;
+  if (CL) {
+    pdl_wait();      // x may be the output of the preceding grid
+    pdl_trigger();
+  }
+  // every CTA of the grid (cluster) has finished the phase before; false after
+  // a timed-out grid barrier (the cluster barrier has no time-out: every CTA
+  // of a cluster is co-scheduled and arrives)
+  auto phase_sync = [&]() -> bool {
+    if (CL) {
+      __syncthreads();
+      cluster_sync();
+      return true;
+    }
+    __syncthreads();
+    if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
+    __syncthreads();
+    return s_ok != 0;
+  };
 
   // ---------------------------------------------- phase 0: logits tiles
   {
@@ -464,10 +492,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
       logits_tile(c, rest / net, rest % net, ks, csm, 256);
     }
   }
-  __syncthreads();
-  if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
-  __syncthreads();
-  if (!s_ok) return;
+  if (!phase_sync()) return;
 
   // ---------------------------------------------- phase 1: top-k, counts
   for (int b = blockIdx.x; b < nb; b += G) {
@@ -503,10 +528,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     __syncthreads();
     for (int e = tid; e < E; e += 256) c.route_hist[(size_t)b * E + e] = cnt[0][e];
   }
-  __syncthreads();
-  if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
-  __syncthreads();
-  if (!s_ok) return;
+  if (!phase_sync()) return;
 
   // ---------------------------------------------- phase 2: per-expert scan
   // (many blocks only; up to kDirectBlocks, phase 3 sums the counts directly)
@@ -534,12 +556,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     if (tid == 255) c.route_hist[(size_t)nb * E + e] = before + incl;   // the expert's total
     __syncthreads();   // warp_tot reuse
   }
-  if (!direct) {
-    __syncthreads();
-    if (tid == 0 && !coop_grid_barrier(bar, (unsigned)G, c.status)) s_ok = 0;
-    __syncthreads();
-    if (!s_ok) return;
-  }
+  if (!direct && !phase_sync()) return;
   for (int e = tid; e < E; e += 256) {   // the experts' totals
     int tot = 0;
     if (direct)
@@ -677,10 +694,16 @@ cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st) {
   FwdCtx cc = c;
   if (!gather) cc.xp = nullptr;
   cc.ksplit = (c.H + kRouteKC - 1) / kRouteKC;
-  cudaError_t e = opt_in_smem((const void*)route_coop_kernel, kLogitSmem);
+  if (c.T <= kRouteClusterMaxT) {
+    cudaError_t e = opt_in_smem((const void*)route_coop_kernel<true>, kLogitSmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(route_coop_kernel<true>, dim3(kRouteClusterCTAs), dim3(256), kLogitSmem, st, kRouteClusterCTAs,
+                      cc);
+  }
+  cudaError_t e = opt_in_smem((const void*)route_coop_kernel<false>, kLogitSmem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;   // all CTAs of the cooperative launch must be co-resident
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel, 256, kLogitSmem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel<false>, 256, kLogitSmem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1 || c.num_sms < 1) return cudaErrorNotSupported;
   // the grid size belongs to the barrier counter the kernel picks (fixed per
@@ -697,5 +720,5 @@ cudaError_t launch_route_gather(const FwdCtx& c, bool gather, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_coop_kernel, cc);
+  return cudaLaunchKernelEx(&cfg, route_coop_kernel<false>, cc);
 }
