@@ -70,13 +70,19 @@ struct Cfg {
   static constexpr int kMats = 2;
   static constexpr int kAcc = kWide ? 1 : 2;          // accumulators
   static constexpr int kHalf = kWide ? 256 : NMAX;    // TMEM column of the second A matrix's half
-  // Warp roles: kDqGroups groups of 8 dequant warps (group g converts the
-  // K steps s with s % kDqGroups == g), then 4 epilogue warps (TMEM lane
-  // quarters 0-3), the int4 producer, the token producer and the MMA warp.
+  // Warp roles: the MMA warp (warp 0), the int4 producer (1), the token
+  // producer (2); in the narrow variant a second MMA warp (3): each issues the
+  // MMAs of one A matrix, because there one thread issuing every MMA of a K
+  // step was the bottleneck (~60 cycles per M = 128, N <= 64 MMA in
+  // isolation, ~160 among busy dequant warps); then 4 epilogue warps (one per
+  // TMEM lane quarter warp % 4), then kDqGroups groups of 8 dequant warps
+  // (group g converts the K steps s with s % kDqGroups == g).
   static constexpr int kDqGroups = kWide ? 1 : 2;
   static constexpr int kDqAll = kDqWarps * kDqGroups;
-  static constexpr int kWarpProd = kDqAll + 4, kWarpProdB = kDqAll + 5, kWarpMma = kDqAll + 6;
-  static constexpr int kThreads = (kDqAll + 7) * 32;
+  static constexpr int kMmaWarps = kTS ? 2 : 1;
+  static constexpr int kWarpMma = 0, kWarpProd = 1, kWarpProdB = 2, kWarpMma2 = 3;
+  static constexpr int kWarpEpi = 2 + kMmaWarps, kWarpDq = kWarpEpi + 4;
+  static constexpr int kThreads = (kWarpDq + kDqAll) * 32;
   // every int4 stage carries its block scales when a group does not see the
   // first K step of every block
   static constexpr bool kScalesEveryStage = kDqGroups > 1;
@@ -253,14 +259,14 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
     }
     for (int s = 0; s < C::kStagesA; ++s) {
       mbar_init(&a_full[s], DENSE ? 1 : kDqWarps);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&a_empty[s], C::kMmaWarps);   // one commit per MMA warp
     }
     for (int s = 0; s < C::kStagesB; ++s) {
       mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+      mbar_init(&b_empty[s], C::kMmaWarps);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_full[s], C::kMmaWarps);
       mbar_init(&acc_empty[s], C::kAcc == 1 ? 12 : 4);   // one arrive per warp that reads the accumulator
     }
     fence_mbar_init();
@@ -427,8 +433,9 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == C::kWarpMma) {
+  } else if (warp == C::kWarpMma || (C::kMmaWarps > 1 && warp == C::kWarpMma2)) {
     // ---------------------------------------------------------------- MMA
+    const int mi = warp == C::kWarpMma ? 0 : 1;   // narrow: the A matrix this warp issues
     if (lane == 0) {
       Ring ra, rb, racc;
       bool ok = true;
@@ -460,14 +467,16 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
             }
             const uint32_t b_base = smem_u32(smem + C::kOffB + rb.i * C::kBBytes) + (uint32_t)j * bsub;
             if constexpr (C::kTS) {
+              // descriptors and TMEM addresses advance by constants within the
+              // chunk (the descriptor's address field holds address / 16; no
+              // carry: shared addresses stay below 2^18)
               const uint32_t a_t = tmem + (uint32_t)(C::kTmemA + ra.i * C::kTmemAStage + h * (kBK / 2));
+              const uint64_t bd0 = sw128_desc(b_base);
+              const uint32_t acc0 = kc != 0;
+              const uint32_t dm = d0 + (uint32_t)(mi * C::kHalf), am = a_t + (uint32_t)(mi * C::kTmemAMat);
 #pragma unroll
-              for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
-                const uint32_t acc = (kc | k16) != 0;
-                umma_f16_ts(d0, a_t + (uint32_t)(k16 * 8), bdesc, idesc, acc);
-                umma_f16_ts(d0 + (uint32_t)C::kHalf, a_t + (uint32_t)(C::kTmemAMat + k16 * 8), bdesc, idesc, acc);
-              }
+              for (int k16 = 0; k16 < kBK / 16; ++k16)
+                umma_f16_ts(dm, am + (uint32_t)(k16 * 8), bd0 + (uint64_t)(k16 * 2), idesc, k16 == 0 ? acc0 : 1u);
             } else {
               const uint32_t a_base = smem_u32(smem + C::kOffA + ra.i * C::kABytes);
 #pragma unroll
@@ -494,21 +503,21 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < C::kDqAll) {
+  } else if (warp >= C::kWarpDq) {
     // ------------------------------------------------------------ dequant
     const int g = lane >> 2, cq = lane & 3;
-    const int dw = warp % kDqWarps, grp = warp / kDqWarps;   // 16-row tile, group
+    const int dw = (warp - C::kWarpDq) % kDqWarps, grp = (warp - C::kWarpDq) / kDqWarps;   // 16-row tile, group
     int seq = 0;                                             // K steps of this CTA so far
     Ring rr, ra, racc;
     bool ok = true;
     Tile pend = {0, 0, 0, 0};   // gate/up: the tile whose epilogue share is still due
     bool have = false;
-    // this warp's third of a gate/up tile's epilogue (warps 0-3 the middle,
+    // this warp's third of a gate/up tile's epilogue (dequant warps 0-3 the middle,
     // 4-7 the last third of the 32-column chunks)
     auto epilogue_share = [&]() -> bool {
       if (!mbar_wait_bounded(&acc_full[racc.i], racc.ph, c.status)) return false;
       tc_fence_after();
-      const int nch = (pend.n + 31) / 32, part = 1 + (warp >> 2);
+      const int nch = (pend.n + 31) / 32, part = 1 + (dw >> 2);
       epilogue_chunks(pend, part * nch / 3, (part + 1) * nch / 3, racc.i);
       tc_fence_before();
       __syncwarp();
@@ -673,7 +682,7 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
     if (!DENSE && ok && have) epilogue_share();   // the last tile
   } else {
     // ----------------------------------------------------------- epilogue
-    // warps 8..11 -> TMEM lane quarters 0..3
+    // warps 3..6 -> TMEM lane quarters 3, 0, 1, 2
     Ring racc;
     for (int t = sch.lo + blockIdx.x;; t += gridDim.x) {
       Tile tl;
