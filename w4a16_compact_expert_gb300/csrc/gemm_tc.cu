@@ -70,16 +70,16 @@ struct Cfg {
   static constexpr int kMats = 2;
   static constexpr int kAcc = kWide ? 1 : 2;          // accumulators
   static constexpr int kHalf = kWide ? 256 : NMAX;    // TMEM column of the second A matrix's half
-  // Warp roles: the MMA warp (warp 0), the int4 producer (1), the token
-  // producer (2); in the narrow variant a second MMA warp (3): each issues the
-  // MMAs of one A matrix, because there one thread issuing every MMA of a K
-  // step was the bottleneck (~60 cycles per M = 128, N <= 64 MMA in
-  // isolation, ~160 among busy dequant warps); then 4 epilogue warps (one per
-  // TMEM lane quarter warp % 4), then kDqGroups groups of 8 dequant warps
-  // (group g converts the K steps s with s % kDqGroups == g).
+  // Warp roles: two MMA warps (0 and 3, each issuing the MMAs of one A
+  // matrix: one thread issuing every MMA of a K step was the bottleneck of
+  // the small-token pipeline, ~60 cycles per M = 128, N <= 64 MMA in
+  // isolation and ~160 among busy dequant warps), the int4 producer (1), the
+  // token producer (2), then 4 epilogue warps (one per TMEM lane quarter
+  // warp % 4), then kDqGroups groups of 8 dequant warps (group g converts
+  // the K steps s with s % kDqGroups == g).
   static constexpr int kDqGroups = kWide ? 1 : 2;
   static constexpr int kDqAll = kDqWarps * kDqGroups;
-  static constexpr int kMmaWarps = kTS ? 2 : 1;
+  static constexpr int kMmaWarps = 2;
   static constexpr int kWarpMma = 0, kWarpProd = 1, kWarpProdB = 2, kWarpMma2 = 3;
   static constexpr int kWarpEpi = 2 + kMmaWarps, kWarpDq = kWarpEpi + 4;
   static constexpr int kThreads = (kWarpDq + kDqAll) * 32;
@@ -478,14 +478,11 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
               for (int k16 = 0; k16 < kBK / 16; ++k16)
                 umma_f16_ts(dm, am + (uint32_t)(k16 * 8), bd0 + (uint64_t)(k16 * 2), idesc, k16 == 0 ? acc0 : 1u);
             } else {
-              const uint32_t a_base = smem_u32(smem + C::kOffA + ra.i * C::kABytes);
+              const uint32_t a_base = smem_u32(smem + C::kOffA + ra.i * C::kABytes + mi * C::kAMat);
+              const uint32_t dm = d0 + (uint32_t)(mi * C::kHalf);
 #pragma unroll
-              for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                const uint64_t bdesc = sw128_desc(b_base + k16 * 32);
-                const uint32_t acc = (kc | k16) != 0;
-                umma_f16_ss(d0, sw128_desc(a_base + k16 * 32), bdesc, idesc, acc);
-                umma_f16_ss(d0 + (uint32_t)C::kHalf, sw128_desc(a_base + C::kAMat + k16 * 32), bdesc, idesc, acc);
-              }
+              for (int k16 = 0; k16 < kBK / 16; ++k16)
+                umma_f16_ss(dm, sw128_desc(a_base + k16 * 32), sw128_desc(b_base + k16 * 32), idesc, (kc | k16) != 0);
             }
             if (++j == kpb || kc == nks - 1) {   // the token stage's last K chunk
               umma_commit(&b_empty[rb.i]);
