@@ -16,7 +16,7 @@ Workloads (--workload):
            I=1408, E=60, top-4, 39 resident experts at permuted slots, -inf
            logit bias for the 21 absent ones; 1.37 GB), default T=8.
   stack    16 OLMoE-shaped layers run in sequence, x <- x + MoE(rmsnorm(x)),
-           T tokens; --sweep times T in {1, 8, 64, 512, 2048} with the decode
+           T tokens; --sweep times T in {1, 8, 16, 24, 32, 48, 64, 128, 512, 2048} with the decode
            kernels and the grouped GEMM forced in turn and reports the
            crossover.
 Metric: MoE-layer tokens/s = layers * T * steps / time.  The default decode
@@ -61,7 +61,7 @@ class Shape:
 
 OLMOE = Shape("OLMoE", 2048, 1024, 64, 8, 64)
 QWEN = Shape("Qwen-MoE", 2048, 1408, 60, 4, 39)
-SWEEP_T = [1, 8, 64, 512, 2048]
+SWEEP_T = [1, 8, 16, 24, 32, 48, 64, 128, 512, 2048]
 
 
 def parse():

@@ -161,7 +161,7 @@ moe_w4a16_status moe_w4a16_create(const moe_w4a16_config* cfg, moe_w4a16_handle*
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device);
   cudaDeviceGetAttribute(&h->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
   h->ksplit_fused = fused_ksplit(c.hidden);
-  h->gemv_max_tokens = 64;
+  h->gemv_max_tokens = 40;   // between the stack sweep's T = 32 (decode kernels faster) and T = 48 (GEMM faster)
   h->packed.assign(c.num_slots, 0);
   h->h_table.assign(c.num_experts, -1);
   const size_t H = c.hidden, I = c.inter, E = c.num_experts, T = c.max_tokens, P = T * c.top_k;

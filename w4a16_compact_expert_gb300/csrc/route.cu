@@ -446,6 +446,7 @@ constexpr int kDirectBlocks = 64;
 // counter round trips, for the few token blocks of 16 < T <= 64.
 constexpr int kRouteClusterCTAs = 8;
 constexpr int kRouteClusterMaxT = 64;
+static_assert(kDirectBlocks * 256 * 4 <= kLogitSmem, "block counts fit the logits tile's shared memory");
 
 template <bool CL>
 __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
@@ -557,10 +558,18 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     __syncthreads();   // warp_tot reuse
   }
   if (!direct && !phase_sync()) return;
+  // Up to kDirectBlocks blocks: every block's counts into shared memory (the
+  // logits tile's space, free since phase 0) with one coalesced pass, so the
+  // totals and each block's bases below are sums over shared memory.
+  int* hist_s = reinterpret_cast<int*>(csm);   // [nb][E], nb * E * 4 <= kLogitSmem
+  if (direct) {
+    for (int i = tid; i < nb * E; i += 256) hist_s[i] = __ldcg(&c.route_hist[i]);
+    __syncthreads();
+  }
   for (int e = tid; e < E; e += 256) {   // the experts' totals
     int tot = 0;
     if (direct)
-      for (int bb = 0; bb < nb; ++bb) tot += __ldcg(&c.route_hist[(size_t)bb * E + e]);
+      for (int bb = 0; bb < nb; ++bb) tot += hist_s[bb * E + e];
     else
       tot = __ldcg(&c.route_hist[(size_t)nb * E + e]);
     s_tot[e] = tot;
@@ -626,7 +635,7 @@ __global__ void __launch_bounds__(256) route_coop_kernel(FwdCtx c) {
     for (int e = tid; e < E; e += 256) {   // the block's first row inside each expert's group
       int base = 0;
       if (direct)
-        for (int bb = 0; bb < b; ++bb) base += __ldcg(&c.route_hist[(size_t)bb * E + e]);
+        for (int bb = 0; bb < b; ++bb) base += hist_s[bb * E + e];
       else
         base = __ldcg(&c.route_hist[(size_t)b * E + e]);
       s_base[e] = base;
