@@ -60,6 +60,12 @@ constexpr uint32_t kTmemCols = 512;
 //      MMA takes A from there; two groups of dequant warps take alternate
 //      stages, a deep int4 ring covers HBM latency, and two accumulators let
 //      one tile's epilogue run under the next tile's MMAs.
+//  128 (prefill, alternative): the 256-token variant's A ring with two
+//      accumulators of 2 x 128 columns (the epilogue of one tile runs under
+//      the next tile's MMAs instead of stalling them: a trace of the 256-token
+//      variant showed the MMA warp waiting 9,000-13,000 cycles for the
+//      accumulator at each tile start) and two groups of dequant warps (each
+//      expert's weights are converted once per 128-token tile).
 template <bool GU, int NMAX>
 struct Cfg {
   static constexpr bool kWide = NMAX > 64;
@@ -68,8 +74,8 @@ struct Cfg {
   // two 128-row A tiles share every token stage: gate and up (gate/up), rows
   // m0 and m0 + 128 of the down matrix (down)
   static constexpr int kMats = 2;
-  static constexpr int kAcc = kWide ? 1 : 2;          // accumulators
-  static constexpr int kHalf = kWide ? 256 : NMAX;    // TMEM column of the second A matrix's half
+  static constexpr int kAcc = NMAX <= 128 ? 2 : 1;    // accumulators
+  static constexpr int kHalf = NMAX <= 128 ? NMAX : 256;   // TMEM column of the second A matrix's half
   // Warp roles: two MMA warps (0 and 3, each issuing the MMAs of one A
   // matrix: one thread issuing every MMA of a K step was the bottleneck of
   // the small-token pipeline, ~60 cycles per M = 128, N <= 64 MMA in
@@ -77,7 +83,7 @@ struct Cfg {
   // token producer (2), then 4 epilogue warps (one per TMEM lane quarter
   // warp % 4), then kDqGroups groups of 8 dequant warps (group g converts
   // the K steps s with s % kDqGroups == g).
-  static constexpr int kDqGroups = kWide ? 1 : 2;
+  static constexpr int kDqGroups = NMAX <= 128 ? 2 : 1;
   static constexpr int kDqAll = kDqWarps * kDqGroups;
   static constexpr int kMmaWarps = 2;
   static constexpr int kWarpMma = 0, kWarpProd = 1, kWarpProdB = 2, kWarpMma2 = 3;
@@ -106,7 +112,7 @@ struct Cfg {
   static constexpr int kFixed = kASmemStages * kABytes + kStagesB * kBBytes + kSchedBytes +
                                 (2 * kStagesA + 2 * kStagesB + 4) * 8 + 16 + 1024;
   static constexpr int kRawFit = (227 * 1024 - kFixed) / (kRawBytes + 16);
-  static constexpr int kStagesRaw = kWide ? 3 : (kRawFit < 16 ? kRawFit : 16);
+  static constexpr int kStagesRaw = NMAX > 128 ? 3 : (kRawFit < 16 ? kRawFit : 16);
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kASmemStages * kABytes;
   static constexpr int kOffRaw = kOffB + kStagesB * kBBytes;
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
       }
       // 32 columns per TMEM load, or 2 x 16 in the narrow variant (whose 23
       // warps leave fewer registers per thread)
-      constexpr int W = C::kWide ? 32 : 16;
+      constexpr int W = C::kThreads > 512 ? 16 : 32;
 #pragma unroll
       for (int sub = 0; sub < 32; sub += W) {
         if (col0 + sub >= et.n) break;
@@ -865,7 +871,10 @@ PoolMaps make_pool_maps(const uint8_t* pool, const SlotLayout& lay, int num_slot
   return pm;
 }
 
-int gemm_tile_tokens(int T, int k, int E) { return (long long)T * k <= 16ll * E ? 32 : 256; }
+int gemm_tile_tokens(int T, int k, int E) {
+  const long long P = (long long)T * k;
+  return P <= 16ll * E ? 32 : P <= 64ll * E ? 128 : 256;
+}
 
 // gate/up and down grouped GEMMs of one token-tile variant (c.tile_tokens
 // must equal NMAX: the routing kernels chunked the experts' rows with it)
@@ -893,13 +902,16 @@ cudaError_t launch_gemm_pair(const FwdCtx& c, const PoolMaps& pm, cudaStream_t s
 cudaError_t launch_gemm_experts(const FwdCtx& c, const PoolMaps& pm, bool gathered, cudaStream_t st,
                                 const StageEvents& se) {
   if (!gemm_shapes_supported(c.H, c.I) || !pm.ok) return cudaErrorNotSupported;
-  if (c.tile_tokens != 32 && c.tile_tokens != 256) return cudaErrorInvalidValue;
+  if (c.tile_tokens != 32 && c.tile_tokens != 128 && c.tile_tokens != 256) return cudaErrorInvalidValue;
   const uint64_t P = (uint64_t)c.T * c.k;
   cudaError_t e = cudaSuccess;
   if (!gathered)
     e = launch_pdl(gather_rows_kernel, dim3((unsigned)((P + kGatherRows - 1) / kGatherRows)), dim3(256), 0, st, 1, c);
   if (e == cudaSuccess) e = record_stage(se, 1, st);
-  if (e == cudaSuccess) e = c.tile_tokens == 32 ? launch_gemm_pair<32>(c, pm, st, se) : launch_gemm_pair<256>(c, pm, st, se);
+  if (e == cudaSuccess)
+    e = c.tile_tokens == 32    ? launch_gemm_pair<32>(c, pm, st, se)
+        : c.tile_tokens == 128 ? launch_gemm_pair<128>(c, pm, st, se)
+                               : launch_gemm_pair<256>(c, pm, st, se);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel, dim3((unsigned)(c.T * ((c.H / 8 + kCombineThreads - 1) / kCombineThreads))),

@@ -103,8 +103,8 @@ cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEve
 // gemm_tc.cu: prefill regime (gather, gate/up GEMM, down GEMM, combine)
 bool gemm_shapes_supported(int H, int I);
 // Token tile of the grouped GEMM for T tokens (routing chunks each expert's
-// rows with it): 128 while the average expert sees at most 64 pairs (the
-// narrow variant: deep int4 ring, two accumulators), else 256.
+// rows with it), by the average pairs per expert: 32 up to 16 (weights
+// through tensor memory), 128 up to 64 (two accumulators), else 256.
 int gemm_tile_tokens(int T, int k, int E);
 
 // TMA maps over the whole slot pool for the grouped GEMM, built once per
