@@ -612,9 +612,9 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
           ra.next(C::kStagesA);
           continue;
         }
-        // the A ring is full at this point: the MMA waits for the previous
-        // tile's epilogue before it takes stage 0 of this one
-        if (C::kAcc == 1 && have && ks == C::kStagesA && !epilogue_share()) {
+        // the previous tile's epilogue share first: the MMA waits for it
+        // before it takes stage 0 of this tile
+        if (C::kAcc == 1 && have && ks == 0 && !epilogue_share()) {
           ok = false;
           break;
         }
