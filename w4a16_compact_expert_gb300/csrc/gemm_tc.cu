@@ -162,6 +162,11 @@ struct Sched {
   int* start;       // [n]
   int* count;       // [n]
   int lo, hi;       // the tiles this launch covers
+  // Tail split (256-token tile): the tiles [F, hi) of the last, partial wave
+  // are taken as two token halves each, virtual tiles [F, vhi) = [F, F + 2 (hi - F)),
+  // so that no CTA runs a whole tile more than the others
+  int F, vhi;
+  bool split;
 };
 
 DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
@@ -198,7 +203,12 @@ DEV_INLINE Sched load_sched(const FwdCtx& c, int* sm) {
 // kernels wrote that prefix into act_tile).
 DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, int mstep, Tile& out) {
   if (s.n <= 0) return false;
-  if (t >= s.hi) return false;
+  if (t >= s.vhi) return false;
+  int half = -1;
+  if (s.split && t >= s.F) {   // a token half of a tail tile
+    half = (t - s.F) & 1;
+    t = s.F + ((t - s.F) >> 1);
+  }
   const int mt = t % mtiles, ct = t / mtiles;
   int lo = 0, hi = s.n - 1;
   while (lo < hi) {   // last u with tile[u] <= ct
@@ -215,6 +225,15 @@ DEV_INLINE bool get_tile(const Sched& s, int t, int mtiles, int mstep, Tile& out
   out.n = b1 - b0;
   out.m0 = mt * mstep;
   out.u = u;
+  if (half >= 0) {
+    const int h0 = out.n >> 1;
+    if (half == 0) {
+      out.n = h0;
+    } else {
+      out.r0 += h0;
+      out.n -= h0;
+    }
+  }
   return true;
 }
 
@@ -298,6 +317,29 @@ __global__ void __launch_bounds__(Cfg<GU, NMAX>::kThreads, 1)
   } else {
     sch.lo = 0;
     sch.hi = sch.n > 0 ? sch.tile[sch.n] * mtiles : 0;
+  }
+  sch.F = sch.vhi = sch.hi;
+  sch.split = false;
+  if (!DENSE && C::kAcc == 1) {
+    // 256-token tile: with R tiles in the last, partial wave (R <= half the
+    // grid), run them as 2R token halves, one per CTA: the kernel then ends
+    // half a tile after the full waves instead of a whole tile (a 256-token
+    // tile's time is mostly its MMAs, which halve).  Only when every tail
+    // tile has at least 32 tokens, so that no half is nearly empty.
+    const int G = (int)gridDim.x, N = sch.hi - sch.lo, R = N % G;
+    if (R > 0 && 2 * R <= G) {
+      const int F = sch.hi - R;
+      bool big = true;
+      for (int t = F + (int)threadIdx.x; t < sch.hi; t += (int)blockDim.x) {
+        Tile tt;
+        if (get_tile(sch, t, mtiles, mstep, tt)) big = big && tt.n >= 32;
+      }
+      if (__syncthreads_and(big)) {
+        sch.split = true;
+        sch.F = F;
+        sch.vhi = F + 2 * R;
+      }
+    }
   }
   const int nacc = C::kAcc;
   // The epilogue of one tile for the calling warp's TMEM lane quarter, 32-column
