@@ -13,20 +13,25 @@
 //            global; one bounded grid barrier; then every CTA reads the logits
 //            and does softmax / top-k, the expert counts and the stable
 //            permutation in shared memory (CTA 0 publishes them).
-//   weights  a CTA owns a contiguous share of the gate/up items (expert,
-//            16-row tile of I) and of the down items (expert, 32-row block of
-//            H).  The producer warp streams them as a ring of equal entries
-//            (a gate tile, an up tile, or the two row tiles of a down item)
-//            with 1-D bulk copies, starting as soon as the active experts are
-//            known; each consumer warp releases an entry once it has read it.
-//   gate/up  group q takes items q, q + NG, ...: gate entry, then up entry,
-//            K split over the group's warps, all (<= 16) tokens of the expert
-//            at once from the x rows staged in shared memory; h = SiLU(g) * u
+//   weights  each CTA owns a list of units (CtaUnits): gate/up items
+//            (expert, 16-row tile of I) and down items (expert, 32 or 64 rows
+//            of H), either a contiguous share of each kind (phase order) or
+//            every G-th unit of one grid-wide order in which an expert's down
+//            items trail its gate/up items by a fixed lag (interleaved
+//            order).  The producer warp streams a CTA's units as a ring of
+//            equal entries (a gate tile, an up tile, or the two row tiles of
+//            a 32-row down block) with 1-D bulk copies, starting as soon as
+//            the active experts are known; each consumer warp releases an
+//            entry once it has read it.
+//   gate/up  group q takes the CTA's units q, q + NG, ...: gate entry, then
+//            up entry, K split over the group's warps, all (<= 16) tokens of
+//            the expert at once from the x rows staged in shared memory; h = SiLU(g) * u
 //            -> global (FP16); the group leader then leaves a note for the
 //            signaller.
 //   down     once every gate/up item of its expert has counted (a bounded
-//            wait on that counter: no grid-wide barrier), the group stages the
-//            expert's h rows and multiplies its two row tiles -> y (FP32).
+//            wait on that counter, usually already met thanks to the lag: no
+//            grid-wide barrier), the group stages the expert's h rows and
+//            multiplies its two row tiles -> y (FP32).
 //   signal   the signaller warp turns batches of gate/up notes into GPU-wide
 //            readiness counts behind one fence per batch, so no compute warp
 //            waits on a fence or an atomic.
@@ -51,7 +56,7 @@ constexpr int kCW = 12;                        // compute warps
 constexpr int kNW = kCW + 2;                   // + producer warp + signaller warp
 constexpr int kFThreads = kNW * 32;
 constexpr int kMB = 16;                        // notes per group mailbox
-constexpr int kDownRows = 32;                  // rows of H per down item (2 tiles)
+constexpr int kDownRows = 32;                  // rows of H per down entry (2 row tiles)
 constexpr int kMaxT = 16;                      // tokens of the fused path (all staged in smem)
 constexpr int kMaxP = kMaxT * 32;
 constexpr int kMaxSlots = 16;                  // ring entries
@@ -65,6 +70,102 @@ constexpr uint32_t kSmemBudget = 226 * 1024;
 // routed to 8 or more experts; otherwise fewer and wider groups spend less on
 // the cross-warp reductions)
 __host__ __device__ inline int fused_group_warps(int T, int k) { return T == 1 && k >= 8 ? 2 : T <= 8 ? 4 : 6; }
+
+// The interleaved unit order (CtaUnits) for 4-warp groups when a gate/up item
+// (16 H int4 values) and a 64-row down item (64 I) move about the same bytes
+// (within 1/8): groups then take equal shares by count.  Measured on the
+// OLMoE shape (H = 2 I): T = 4 35.1 against 38.0 us per layer in the phase
+// order, T = 2 27.1 against 29.6; with 2- or 6-warp groups the phase order
+// was faster (T = 1, 16), as it was on the Qwen shape (H = 2048, I = 1408),
+// whose down items are larger.
+inline int fused_interleaved(int H, int I, int gw) {
+  const long long gu = 16ll * H, dn = 32ll * I, d = gu > dn ? gu - dn : dn - gu;
+  return gw == 4 && 8 * d <= gu;
+}
+
+// The grid's unit order.  A unit is a gate/up item (expert, 16-row tile of I:
+// a gate entry and an up entry) or a down item (expert, 64-row block of H:
+// two entries of 2 row tiles); both move about the same bytes.  The units
+// form blocks j = 0 .. U + L - 1: block j holds the down items of active
+// expert j - L (when 0 <= j - L < U), then the gate/up items of active expert
+// j (when j < U).  Unit x belongs to CTA x % G, whose groups take its units
+// in turn, so the grid works through the order front to back: one expert's
+// gate/up items run side by side in different CTAs, and its down items come
+// L blocks later, when they are usually ready.  No grid-wide phase separates
+// gate/up from down, and the weight stream does not pause between them.
+// Every unit depends
+// only on units earlier in the order, each CTA holds its units in that order
+// and each group takes them in it, so the first unfinished unit of the grid
+// can always proceed: no deadlock.
+// L: the gate/up items of L - 1 experts (t1 each) span kLagQ quarters of one
+// step of the grid's groups (G x NG units), so every expert's gate/up items
+// have finished, and been counted, about that long before its first down item
+// starts (the groups start together, so this covers the first experts too).
+constexpr int kLagQ = 10;
+struct UnitOrder {
+  int U, L, t1, t2;
+};
+struct Unit {
+  int down, u, idx;
+};
+__host__ __device__ inline UnitOrder unit_order(int U, int t1, int t2, int G, int NG) {
+  return UnitOrder{U, 1 + (kLagQ * G * NG + 4 * t1 - 1) / (4 * t1), t1, t2};
+}
+__host__ __device__ inline Unit unit_at(const UnitOrder& o, int x) {
+  const int r1 = (o.L < o.U ? o.L : o.U) * o.t1;   // blocks before L: gate/up items only
+  if (x < r1) return Unit{0, x / o.t1, x % o.t1};
+  x -= r1;
+  const int nmix = o.U > o.L ? o.U - o.L : 0, bs = o.t1 + o.t2;
+  if (x < nmix * bs) {
+    const int jj = x / bs, r = x - jj * bs;
+    return r < o.t2 ? Unit{1, jj, r} : Unit{0, o.L + jj, r - o.t2};
+  }
+  x -= nmix * bs;   // blocks from max(U, L): down items only
+  return Unit{1, nmix + x / o.t2, x % o.t2};
+}
+
+// The units of CTA b, in the order its producer streams them and its groups
+// (group q: units q, q + NG, ...) take them.  Two orders:
+//   interleaved  x = b + j G of the unit order above; down items of 64 rows
+//                of H (two entries), so both kinds move about the same bytes
+//                when 16 H ~ 32 I;
+//   phases       a contiguous share of the gate/up items, then a contiguous
+//                share of the down items (32 rows of H: one entry); every
+//                CTA reaches its down items about when the whole grid's
+//                gate/up items finish, but a group's consecutive down items
+//                mostly share an expert, whose h rows it stages once.
+template <bool INTER>
+struct CtaUnits {
+  static constexpr bool inter = INTER;
+  UnitOrder ord;
+  int NU, b, G;                 // interleaved
+  int a1, m1, a2, m2, t1, t2;   // phases (t2: 32-row down items per expert)
+  DEV_INLINE int count() const { return inter ? (NU > b ? (NU - b + G - 1) / G : 0) : m1 + m2; }
+  DEV_INLINE Unit at(int j) const {
+    if (inter) return unit_at(ord, b + j * G);
+    if (j < m1) return Unit{0, (a1 + j) / t1, (a1 + j) % t1};
+    return Unit{1, (a2 + j - m1) / t2, (a2 + j - m1) % t2};
+  }
+  DEV_INLINE int first_entry(int j) const { return inter || j < m1 ? 2 * j : 2 * m1 + (j - m1); }
+  DEV_INLINE int down_entries() const { return inter ? 2 : 1; }
+  DEV_INLINE int down_block(const Unit& un, int sub) const { return inter ? 2 * un.idx + sub : un.idx; }   // 32-row block of H
+};
+template <bool INTER>
+DEV_INLINE CtaUnits<INTER> cta_units(int U, int I, int H, int b, int G, int NG) {
+  CtaUnits<INTER> cu;
+  cu.b = b;
+  cu.G = G;
+  cu.t1 = I / 16;
+  cu.t2 = H / kDownRows;
+  cu.ord = unit_order(U, cu.t1, H / (2 * kDownRows), G, NG);
+  cu.NU = U * (cu.t1 + H / (2 * kDownRows));
+  const int n1 = U * cu.t1, n2 = U * cu.t2;
+  cu.a1 = (int)((long long)b * n1 / G);
+  cu.m1 = (int)((long long)(b + 1) * n1 / G) - cu.a1;
+  cu.a2 = (int)((long long)b * n2 / G);
+  cu.m2 = (int)((long long)(b + 1) * n2 / G) - cu.a2;
+  return cu;
+}
 
 struct FusedSmem {
   uint32_t ns, slot_bytes, off_x, off_h, off_red, off_sb, off_route, total;
@@ -447,7 +548,7 @@ DEV_INLINE void post_note(int* mbox, volatile int* head, volatile int* tail, int
   *head = ++my_head;
 }
 
-template <int GW>
+template <int GW, bool INTER>
 __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   constexpr int NG = kCW / GW;
   constexpr int kMatUnroll = GW == 6 ? 2 : 1;
@@ -456,6 +557,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   __shared__ int s_ok;
   __shared__ volatile int s_abort;   // a bounded wait ran out: stop waiting
   __shared__ volatile int s_seq[kMaxSlots];   // entry held by each ring slot
+  __shared__ CtaUnits<INTER> s_cu;            // the CTA's units (compute warps and signaller)
   __shared__ int s_mbox[NG][kMB];             // group -> signaller notes
   __shared__ volatile int s_head[NG], s_tail[NG];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -571,7 +673,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
     }
   }
   __syncthreads();   // top-k ids and weights of every token
-  const int tpe1 = I / 16, tpe2 = H / kDownRows;
+  const int tpe1 = I / 16;   // gate/up items per expert
 
   if (warp == kCW) {
     // ------------------------------------------------------------ producer
@@ -593,41 +695,47 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       U += __popc(am);
     }
     __syncwarp();
-    const int n1 = U * tpe1, n2 = U * tpe2;
-    const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
-    const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
-    // entries: 2j (gate tile) and 2j + 1 (up tile) of gate/up item j < m1,
-    // then 2 m1 + j (the 2 row tiles of down item j < m2); entry e -> slot e % NS
+    const CtaUnits<INTER> cu = cta_units<INTER>(U, I, H, b, G, NG);
+    // the CTA's units in order: a gate/up item is a gate entry and an up
+    // entry, a down item one or two entries of a 32-row block (2 row tiles);
+    // entry e -> slot e % NS
     if (lane == 0) {
-      const int ne = 2 * m1 + m2;
       int issued = 0;
-      for (int e = 0; e < ne; ++e) {
-        const int s = e % NS;
-        if (!wait_phase(&empty[s], (uint32_t)((e / NS) & 1) ^ 1u, &s_abort, c.status)) break;
-        // at most kInFlight entries on their way: copies issued together share
-        // the bandwidth and land together, so a bounded window lets the first
-        // entries land (and compute start) early.  Entry e - kInFlight's slot
-        // cannot hold a newer entry yet, so its parity is unambiguous.
-        if (e >= kInFlight) {
-          const int ep = e - kInFlight;
-          if (!wait_phase(&full[ep % NS], (uint32_t)((ep / NS) & 1), &s_abort, c.status)) break;
+      bool stop = false;
+      const int nu = cu.count();
+      for (int j = 0; j < nu && !stop; ++j) {
+        const Unit un = cu.at(j);
+        const uint8_t* base = c.pool + (size_t)r_aslot[un.u] * c.slot_bytes;
+        for (int sub = 0; sub < (un.down ? cu.down_entries() : 2); ++sub) {
+          const int e = issued, s = e % NS;
+          if (!wait_phase(&empty[s], (uint32_t)((e / NS) & 1) ^ 1u, &s_abort, c.status)) {
+            stop = true;
+            break;
+          }
+          // at most kInFlight entries on their way: copies issued together share
+          // the bandwidth and land together, so a bounded window lets the first
+          // entries land (and compute start) early.  Entry e - kInFlight's slot
+          // cannot hold a newer entry yet, so its parity is unambiguous.
+          if (e >= kInFlight) {
+            const int ep = e - kInFlight;
+            if (!wait_phase(&full[ep % NS], (uint32_t)((ep / NS) & 1), &s_abort, c.status)) {
+              stop = true;
+              break;
+            }
+          }
+          s_seq[s] = e;
+          uint8_t* dst = sm + (size_t)s * L.slot_bytes;
+          if (!un.down) {
+            const MatLayout& M = sub ? c.lay.up : c.lay.gate;
+            mbar_expect_tx(&full[s], M.tile_bytes);
+            bulk_g2s(dst, tile_ptr(base, M, un.idx), M.tile_bytes, &full[s]);
+          } else {
+            const uint32_t bytes = 2 * c.lay.down.tile_bytes;   // the 2 row tiles of a block are contiguous
+            mbar_expect_tx(&full[s], bytes);
+            bulk_g2s(dst, tile_ptr(base, c.lay.down, 2 * cu.down_block(un, sub)), bytes, &full[s]);
+          }
+          issued = e + 1;
         }
-        s_seq[s] = e;
-        uint8_t* dst = sm + (size_t)s * L.slot_bytes;
-        if (e < 2 * m1) {
-          const int it = a1 + (e >> 1), u = it / tpe1, rt = it % tpe1;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const MatLayout& M = (e & 1) ? c.lay.up : c.lay.gate;
-          mbar_expect_tx(&full[s], M.tile_bytes);
-          bulk_g2s(dst, tile_ptr(base, M, rt), M.tile_bytes, &full[s]);
-        } else {
-          const int it = a2 + (e - 2 * m1), u = it / tpe2, hb = it % tpe2;
-          const uint8_t* base = c.pool + (size_t)r_aslot[u] * c.slot_bytes;
-          const uint32_t bytes = 2 * c.lay.down.tile_bytes;   // the 2 row tiles of a block are contiguous
-          mbar_expect_tx(&full[s], bytes);
-          bulk_g2s(dst, tile_ptr(base, c.lay.down, 2 * hb), bytes, &full[s]);
-        }
-        issued = e + 1;
       }
       // copies in flight land before the CTA (and its shared memory) ends:
       // only the last entry issued into a slot can still be pending
@@ -684,20 +792,24 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       n += __popc(am);
       base += __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 0) r_off[E] = base;
-    if (lane == 0) r_misc[0] = n;
+    if (lane == 0) {
+      r_off[E] = base;
+      r_misc[0] = n;
+      s_cu = cta_units<INTER>(n, I, H, b, G, NG);
+    }
   }
   named_sync(6, (kNW - 1) * 32);
   const int U = r_misc[0];
-  const int n1 = U * tpe1, n2 = U * tpe2;
-  const int a1 = (int)((long long)b * n1 / G), m1 = (int)((long long)(b + 1) * n1 / G) - a1;
-  const int a2 = (int)((long long)b * n2 / G), m2 = (int)((long long)(b + 1) * n2 / G) - a2;
+  const CtaUnits<INTER>& cu = s_cu;
 
   if (warp == kCW + 1) {
     // ----------------------------------------------------------- signaller
     // Turns the groups' gate/up notes into GPU-wide readiness counts, one
     // fence per batch of notes, the adds fire-and-forget.
     unsigned* ready = c.expert_ready;
+    int m1 = 0;   // the CTA's gate/up items: one note each
+    for (int j = lane; j < cu.count(); j += 32) m1 += 1 - cu.at(j).down;
+    m1 = __reduce_add_sync(kFull, m1);
     int processed = 0, tails[NG];
 #pragma unroll
     for (int q = 0; q < NG; ++q) tails[q] = 0;
@@ -780,10 +892,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   int ready_u = -1, staged_u = -1, staged_p0 = -1;
   int my_head = 0;                           // leader: notes posted
 
-  for (int i = q; i < m1 + m2; i += NG) {
-    if (i < m1) {
+  const int nu = cu.count();
+  for (int j = q; j < nu; j += NG) {   // the CTA's units q, q + NG, ...
+    const Unit un = cu.at(j);
+    const int e0 = cu.first_entry(j);
+    if (!un.down) {
       // ---------------------------------------------------- gate/up item
-      const int it = a1 + i, u = it / tpe1, rt = it % tpe1;
+      const int u = un.u, rt = un.idx;
       const int start = r_astart[u], cnt = r_acount[u];   // cnt <= T <= 16
       const int ntl = cnt > 8 ? 2 : 1;
       const int tok0 = r_sorted[start] / k;
@@ -812,7 +927,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
-        const int e = 2 * i + mat, s = e % NS;
+        const int e = e0 + mat, s = e % NS;
         warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
         const uint8_t* tile = sm + (size_t)s * L.slot_bytes;
         if (ntl == 1)
@@ -855,58 +970,61 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
       if (gtid == 0) post_note(&s_mbox[q][0], &s_head[q], &s_tail[q], my_head, u, &s_abort, c.status);
     } else {
       // ------------------------------------------------------- down item
-      const int j2 = i - m1, it = a2 + j2, u = it / tpe2, hb = it % tpe2;
+      const int u = un.u;
       const int start = r_astart[u], cnt = r_acount[u];
-      const int e = 2 * m1 + j2, s = e % NS;
       if (u != ready_u) {   // h of expert u complete (every gate/up item counted)
         if (gtid == 0) wait_count(&ready[u], (unsigned)tpe1, &s_abort, c.status);
         ready_u = u;
       }
-      const int tl = wq & 1, ks = wq >> 1;   // row tile of the entry, K part
-      const uint8_t* tile = sm + (size_t)s * L.slot_bytes + (size_t)tl * c.lay.down.tile_bytes;
-      warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
-      for (int p0 = 0; p0 < cnt; p0 += kTok) {
-        const int np = min(kTok, cnt - p0);
-        float* sbg = sb_h + (size_t)q * (T < kTok ? T : kTok) * (I / 64 + 1);   // this group's h prefix sums
-        if (u != staged_u || p0 != staged_p0) {
-          named_sync(gbar, GW * 32);   // readiness seen by the leader; the group is done with hs
-          const int vpr = I / 8;       // the np rows are consecutive in hbuf
-          const __half* src = c.hbuf + (size_t)(start + p0) * I;
-          for (int v = gtid; v < np * vpr; v += GW * 32)
-            cp_async16(hs + (size_t)(v / vpr) * (I + 8) + (v % vpr) * 8, src + (size_t)v * 8);
-          cp_async_wait_all();
+      const int tl = wq & 1, ks = wq >> 1;   // row tile of an entry, K part
+#pragma unroll 1
+      for (int sub = 0; sub < cu.down_entries(); ++sub) {   // the item's 32-row blocks, one entry each
+        const int hb = cu.down_block(un, sub), e = e0 + sub, s = e % NS;
+        const uint8_t* tile = sm + (size_t)s * L.slot_bytes + (size_t)tl * c.lay.down.tile_bytes;
+        warp_wait_entry(s_seq, full, e, NS, &s_abort, c.status, lane);
+        for (int p0 = 0; p0 < cnt; p0 += kTok) {
+          const int np = min(kTok, cnt - p0);
+          float* sbg = sb_h + (size_t)q * (T < kTok ? T : kTok) * (I / 64 + 1);   // this group's h prefix sums
+          if (u != staged_u || p0 != staged_p0) {
+            named_sync(gbar, GW * 32);   // readiness seen by the leader; the group is done with hs
+            const int vpr = I / 8;       // the np rows are consecutive in hbuf
+            const __half* src = c.hbuf + (size_t)(start + p0) * I;
+            for (int v = gtid; v < np * vpr; v += GW * 32)
+              cp_async16(hs + (size_t)(v / vpr) * (I + 8) + (v % vpr) * 8, src + (size_t)v * 8);
+            cp_async_wait_all();
+            named_sync(gbar, GW * 32);
+            chunk_sums(sbg, hs, I + 8, np, I / 64, gtid, GW * 32);
+            named_sync(gbar, GW * 32);
+            chunk_prefix(sbg, np, I / 64, gtid, GW * 32);
+            staged_u = u;
+            staged_p0 = p0;
+          }
+          named_sync(gbar, GW * 32);   // staged rows and sums visible; previous pass done with rg
+          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          const __half* const brow[2] = {hs + (size_t)(g < np ? g : 0) * (I + 8), hs};
+          const int nki = I / 64, parts = GW / 2;
+          const float* const pre[2][2] = {{sbg + (size_t)(2 * cc < np ? 2 * cc : 0) * (nki + 1),
+                                           sbg + (size_t)(2 * cc + 1 < np ? 2 * cc + 1 : 0) * (nki + 1)},
+                                          {sbg, sbg}};
+          mma_range<1>(acc, tile, c.lay.down.scale_bytes, brow, pre, lane, ks * nki / parts, (ks + 1) * nki / parts);
+          float* rw = rg + wq * 16 * kTok;
+          rw[g * kTok + 2 * cc] = acc[0][0];
+          rw[g * kTok + 2 * cc + 1] = acc[0][1];
+          rw[(g + 8) * kTok + 2 * cc] = acc[0][2];
+          rw[(g + 8) * kTok + 2 * cc + 1] = acc[0][3];
           named_sync(gbar, GW * 32);
-          chunk_sums(sbg, hs, I + 8, np, I / 64, gtid, GW * 32);
-          named_sync(gbar, GW * 32);
-          chunk_prefix(sbg, np, I / 64, gtid, GW * 32);
-          staged_u = u;
-          staged_p0 = p0;
-        }
-        named_sync(gbar, GW * 32);   // staged rows and sums visible; previous pass done with rg
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const __half* const brow[2] = {hs + (size_t)(g < np ? g : 0) * (I + 8), hs};
-        const int nki = I / 64, parts = GW / 2;
-        const float* const pre[2][2] = {{sbg + (size_t)(2 * cc < np ? 2 * cc : 0) * (nki + 1),
-                                         sbg + (size_t)(2 * cc + 1 < np ? 2 * cc + 1 : 0) * (nki + 1)},
-                                        {sbg, sbg}};
-        mma_range<1>(acc, tile, c.lay.down.scale_bytes, brow, pre, lane, ks * nki / parts, (ks + 1) * nki / parts);
-        float* rw = rg + wq * 16 * kTok;
-        rw[g * kTok + 2 * cc] = acc[0][0];
-        rw[g * kTok + 2 * cc + 1] = acc[0][1];
-        rw[(g + 8) * kTok + 2 * cc] = acc[0][2];
-        rw[(g + 8) * kTok + 2 * cc + 1] = acc[0][3];
-        named_sync(gbar, GW * 32);
-        for (int idx = gtid; idx < kDownRows * np; idx += GW * 32) {
-          const int tok = idx / kDownRows, row = idx % kDownRows, t16 = row >> 4, r16 = row & 15;
-          float y = 0.f;
+          for (int idx = gtid; idx < kDownRows * np; idx += GW * 32) {
+            const int tok = idx / kDownRows, row = idx % kDownRows, t16 = row >> 4, r16 = row & 15;
+            float y = 0.f;
 #pragma unroll
-          for (int kp = 0; kp < GW / 2; ++kp) y += rg[(kp * 2 + t16) * 16 * kTok + r16 * kTok + tok];
-          c.ybuf[(size_t)r_sorted[start + p0 + tok] * H + hb * kDownRows + row] = y;
+            for (int kp = 0; kp < GW / 2; ++kp) y += rg[(kp * 2 + t16) * 16 * kTok + r16 * kTok + tok];
+            c.ybuf[(size_t)r_sorted[start + p0 + tok] * H + hb * kDownRows + row] = y;
+          }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
 
@@ -929,12 +1047,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_decode_kernel(FwdCtx c) {
   }
 }
 
-template <int GW>
+template <int GW, bool INTER>
 cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
-  cudaError_t e = opt_in_smem((const void*)fused_decode_kernel<GW>, L.total);
+  cudaError_t e = opt_in_smem((const void*)fused_decode_kernel<GW, INTER>, L.total);
   if (e != cudaSuccess) return e;
   int per_sm = 0;   // all CTAs of a cooperative launch must be co-resident
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel<GW>, kFThreads, L.total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel<GW, INTER>, kFThreads, L.total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
@@ -953,12 +1071,12 @@ cudaError_t launch_fused(const FwdCtx& c, const FusedSmem& L, cudaStream_t st) {
   cfg.attrs = attr;
   static std::atomic<int> pdl_ok{1};   // cleared if the driver refuses the pair of attributes
   cfg.numAttrs = pdl_ok.load() ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+  e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW, INTER>, c);
   if (e != cudaSuccess && cfg.numAttrs == 2) {
     cudaGetLastError();
     pdl_ok.store(0);
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW>, c);
+    e = cudaLaunchKernelEx(&cfg, fused_decode_kernel<GW, INTER>, c);
   }
   return e;
 }
@@ -977,7 +1095,11 @@ bool fused_decode_supported(const FwdCtx& c, int max_smem) {
 cudaError_t launch_fused_decode(const FwdCtx& c, cudaStream_t st, const StageEvents& se) {
   const FusedSmem L = fused_smem(c.lay, c.H, c.I, c.E, c.T, c.k, fused_group_warps(c.T, c.k));
   const int gw = fused_group_warps(c.T, c.k);
-  cudaError_t e = gw == 2 ? launch_fused<2>(c, L, st) : gw == 4 ? launch_fused<4>(c, L, st) : launch_fused<6>(c, L, st);
+  // the interleaved order is instantiated for 4-warp groups only
+  cudaError_t e = gw == 2   ? launch_fused<2, false>(c, L, st)
+                  : gw == 6 ? launch_fused<6, false>(c, L, st)
+                  : fused_interleaved(c.H, c.I, gw) ? launch_fused<4, true>(c, L, st)
+                                                    : launch_fused<4, false>(c, L, st);
   if (e == cudaSuccess) e = record_stage(se, 2, st);
   if (e == cudaSuccess) e = record_stage(se, 3, st);
   if (e == cudaSuccess) e = record_stage(se, 4, st);

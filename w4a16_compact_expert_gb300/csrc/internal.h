@@ -49,7 +49,7 @@ struct FwdCtx {
   unsigned long long* route_bar;  // [2] grid-barrier counters of the cooperative router (monotonic; one grid size each)
   unsigned* down_counters;     // [H/32] arrival counters (self-resetting)
   unsigned long long* grid_bar;  // grid-barrier arrivals (monotonic, a multiple of the grid between uses)
-  unsigned* expert_ready;      // [2][256] per active expert: finished gate/up items, started down items
+  unsigned* expert_ready;      // [2][256]: [u] finished gate/up items of active expert u (the fused kernel); the rest unused
   DevStatus* status;
   int num_sms;
   int max_active;              // upper bound of active experts: min(E, T*k)
