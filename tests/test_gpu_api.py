@@ -104,6 +104,37 @@ def test_routed_absent_expert_counts_misses(tiny, flags):
     gp.assert_output(out, ref.out, keep)
 
 
+@pytest.mark.parametrize("name,T,absent", [("tiny", 6, (3, 6)), ("olmoe", 8, tuple(range(0, 64, 5))),
+                                           ("olmoe", 16, tuple(range(2, 64, 5)))])
+@pytest.mark.parametrize("flags", [0, F.RESIDUAL])
+def test_fused_kernel_routed_absent_experts(name, T, absent, flags):
+    """Routed experts without a slot on the single-launch decode kernel, in
+    both of its unit orders: TINY at T = 6 and OLMoE at T = 8 run the
+    interleaved order (OLMoE with 30 active experts, past the lag, so down
+    items and gate/up items alternate), OLMoE at T = 16 the phase order.  The
+    pairs routed to absent experts count as misses and add nothing; the rest
+    matches the oracle."""
+    layer = synth.tiny_layer() if name == "tiny" else synth.olmoe_decode_layer()
+    x = synth.draw_x(31 + T, T, layer.shape.hidden)
+    table = layer.expert_to_slot.copy()
+    table[list(absent)] = -1
+    m = gp.make_handle(layer, 16)
+    try:
+        m.set_slot_table(table)
+        out, _ = gp.gpu_forward(m, layer, x, flags)
+        path = m.last_path()
+        st, miss = m.get_status()
+    finally:
+        m.close()
+    ref = moe_oracle.moe_layer(x, layer.router_w, layer.bias, layer.slot_experts().arrays(), layer.shape.top_k,
+                               flags, expert_to_slot=table)
+    expected_miss = int(np.isin(ref.ids, absent).sum())
+    assert expected_miss > 0
+    assert path == (F.PATH_DECODE_FUSED, 1)
+    assert st == F.ERR_NOT_RESIDENT and miss == expected_miss
+    gp.assert_output(out, ref.out, ~ref.near_tie)
+
+
 def test_dense_single_expert_and_k_equals_e():
     shape = synth.LayerShape(hidden=128, inter=64, num_experts=1, top_k=1)
     layer = synth.make_layer(shape, 5)
